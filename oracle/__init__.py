@@ -1,0 +1,17 @@
+"""Float64 CPU oracle for paged decode attention.
+
+Test infrastructure: only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may use it.  The CUDA path never imports it.
+Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle.py``.
+"""
+from .paged_attention import (  # noqa: F401
+    BLOCK_SIZE,
+    append_ref,
+    as_f64,
+    attend,
+    bf16_bits_to_f64,
+    decode_ref,
+    gather_contiguous,
+    kv_cache_bytes,
+    prefill_ref,
+)
