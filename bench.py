@@ -1,0 +1,425 @@
+"""Benchmark of the paged-decode hot path on GB300.
+
+One step = one decode step of the Llama-3-8B-shaped batch-64 workload (h_q 32,
+h_kv 8, D 128, bf16, contexts log-uniform in [512, 8192]): append every
+sequence's new K/V through the slot mapping, then paged decode attention
+(split-K + log-sum-exp combine).  Step t of the timed loop uses the inputs of
+workload step t mod 32, so contexts grow by one token per step as in decoding.
+
+Printed JSON (rank 0): value = effective HBM GB/s of the whole step
+(algorithmic bytes of append + attention / device time), with the attention
+call's own roofline, an end-to-end figure through the public API with host
+buffers, the CPU oracle as a baseline, and SM clocks sampled while the GPU
+was busy.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: effective HBM GB/s (% of GB300 peak), decode tokens/s"
+WORKLOAD = "llama3_8b_decode"
+WORKLOAD_DESC = ("Llama-3-8B-shaped paged decode: batch 64, h_q 32, h_kv 8, d_head 128, bf16, block 16, "
+                 "contexts log-uniform in [512, 8192], randomly permuted pool (1.25x need), 32 decode steps "
+                 "each appending one token per sequence")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["paged_kv_decode_27_gb300/csrc/decode_tc.cu", "paged_kv_decode_27_gb300/csrc/combine.cu",
+                  "paged_kv_decode_27_gb300/csrc/decode_merge.cuh", "paged_kv_decode_27_gb300/csrc/pa_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--partition", type=int, default=0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(units_ratio: float):
+    """DRAM bytes per attention call from the committed ncu summary, scaled
+    from its captured case to this one by the K/V bytes processed; None when
+    the kernel sources changed since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_sha") != kernel_sha():
+        return None
+    return float(rec["dram_bytes_per_call"]) * units_ratio if rec.get("scale_with_kv") else \
+        float(rec["dram_bytes_per_call"])
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 <= t <= t1] or [p for _, p in self.samples]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(p[1]) for p in win if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for p in win if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in win:
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+def cpu_baseline(max_seconds: float = 20.0):
+    """Time the float64 CPU oracle on a bounded sample of the workload (step 0,
+    sequences in order until max_seconds), in a fresh 1-thread process."""
+    code = r"""
+import json, os, sys, time
+sys.path.insert(0, %r)
+import torch
+torch.set_num_threads(1)
+import oracle
+from paged_kv_decode_27_gb300 import workloads as W
+wl = W.%s()
+st = wl.step(0)
+def npv(t):
+    t = t.contiguous()
+    return t.view(torch.int16).numpy().view('uint16') if t.dtype == torch.bfloat16 else t.numpy()
+kp, vp = oracle.append_ref(npv(wl.k_pool), npv(wl.v_pool), st.slot_mapping.numpy(), npv(st.k_new), npv(st.v_new))
+bt = wl.decode_block_tables.contiguous().numpy(); ctx = st.context_lens.numpy(); q = npv(st.q)
+done = []; t0 = time.perf_counter()
+for s in range(len(ctx)):
+    oracle.decode_ref(q, kp, vp, bt, ctx, wl.scale, seqs=[s])
+    done.append(s)
+    if time.perf_counter() - t0 > %f: break
+el = time.perf_counter() - t0
+e = 2; hkv, d, hq = wl.num_kv_heads, wl.head_dim, wl.num_q_heads
+b = sum(int(ctx[s]) * 2 * hkv * d * e + 2 * hq * d * e + 4 * ((int(ctx[s]) + 15) // 16) + 4 for s in done)
+print(json.dumps({"seconds": el, "seqs": len(done), "bytes": b, "tokens": sum(int(ctx[s]) for s in done)}))
+""" % (ROOT, WORKLOAD, max_seconds)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
+    rec = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": rec["bytes"] / rec["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"float64 numpy oracle, step 0 of {WORKLOAD}: first {rec['seqs']} of 64 sequences "
+                      f"({rec['tokens']} context tokens, all 32 q heads) in {rec['seconds']:.2f} s, 1 thread",
+            "seconds": rec["seconds"]}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    torch.set_num_threads(1)
+    import oracle
+    from paged_kv_decode_27_gb300 import workloads as W
+    wl = W.llama3_8b_decode()
+
+    def npv(t):
+        t = t.contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+    kp, vp = npv(wl.k_pool), npv(wl.v_pool)
+    bt = wl.decode_block_tables.contiguous().numpy()
+    per_step = 2   # sequences of the batch per step: a bounded sample
+
+    def one(i):
+        st = wl.step(i % wl.steps)
+        seqs = [(2 * i + j) % 64 for j in range(per_step)]
+        k2, v2 = oracle.append_ref(kp, vp, st.slot_mapping.numpy()[seqs], npv(st.k_new)[seqs],
+                                   npv(st.v_new)[seqs])
+        ctx = st.context_lens.numpy()
+        t0 = time.perf_counter()
+        oracle.decode_ref(npv(st.q), k2, v2, bt, ctx, wl.scale, seqs=seqs)
+        el = time.perf_counter() - t0
+        b = sum(int(ctx[s]) * 2 * 8 * 128 * 2 + 2 * 32 * 128 * 2 + 4 * ((int(ctx[s]) + 15) // 16) + 4 for s in seqs)
+        return el, b, seqs
+    for i in range(args.warmup):
+        one(i)
+    tot_t = tot_b = 0.0
+    for i in range(args.steps):
+        el, b, _ = one(args.warmup + i)
+        tot_t += el
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD_DESC},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"float64 numpy oracle: {per_step} sequences (all 32 q heads, their full "
+                                       f"contexts) of each step's batch, rotating; append of those sequences "
+                                       f"untimed"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_decode_27_gb300 import binding as pa
+    from paged_kv_decode_27_gb300 import workloads as W
+
+    # the CPU oracle baseline runs first, in its own 1-thread process
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.llama3_8b_decode()
+    S, hq, hkv, d = wl.num_decode_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    kp, vp = wl.k_pool.to(dev), wl.v_pool.to(dev)
+    bt_cpu = wl.decode_block_tables.contiguous()
+    bt = bt_cpu.to(dev)
+    steps_in = [wl.step(t) for t in range(wl.steps)]
+    dev_in = [(s.slot_mapping.to(dev), s.k_new.to(dev), s.v_new.to(dev), s.q.to(dev), s.context_lens.to(dev))
+              for s in steps_in]
+    max_ctx = wl.max_context_len(wl.steps - 1)
+    part = pa.pa_decode_partition_size(S, max_ctx, kp, args.partition)
+    ws = torch.empty(max(1, pa.pa_decode_workspace_size(S, hq, max_ctx, kp, args.partition)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((S, hq, d), dtype=wl.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    max_splits = -(-((max_ctx + 15) // 16) // (part // 16))
+    launches_per_step = 2 + (1 if max_splits > 1 else 0)
+
+    def step(i):
+        slots, kn, vn, q, ctx = dev_in[i % wl.steps]
+        pa.pa_append_kv(kp, vp, slots, kn, vn, stream=stream)
+        pa.pa_decode_attention(out, q, kp, vp, bt, ctx, wl.scale, max_context_len=max_ctx,
+                               partition_size=args.partition, workspace=ws, stream=stream)
+
+    # untimed: >= 1 s of steps so the clock sampler sees the GPU under load, then W warm-ups
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_busy0 = time.time()
+    i = 0
+    while time.time() - t_busy0 < 1.0:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    # timed: exactly K steps, events on the launching stream around each call
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for k in range(args.steps):
+        t = args.warmup + k
+        slots, kn, vn, q, ctx = dev_in[t % wl.steps]
+        ev[k][0].record(stream)
+        pa.pa_append_kv(kp, vp, slots, kn, vn, stream=stream)
+        ev[k][1].record(stream)
+        pa.pa_decode_attention(out, q, kp, vp, bt, ctx, wl.scale, max_context_len=max_ctx,
+                               partition_size=args.partition, workspace=ws, stream=stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    attn_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    app_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    dec_b = [wl.decode_bytes((args.warmup + k) % wl.steps) for k in range(args.steps)]
+    app_b = wl.append_bytes()
+    step_bytes = sum(dec_b) + args.steps * app_b
+    value = world * step_bytes / (total_ms * 1e-3) / 1e9
+    ms_per_step = total_ms / args.steps
+    peak, peak_kind = peak_hbm()
+    attn_avg_ms = statistics.mean(attn_ms)
+    achieved = statistics.mean(dec_b) / (attn_avg_ms * 1e-3) / 1e9
+    kv_ratio = statistics.mean(dec_b) / wl.decode_bytes(0)
+
+    # e2e through the public API with host buffers: pinned H2D of the step's
+    # inputs (q, new K/V, slots, context lengths, block tables), the two calls,
+    # D2H of the attention output, synchronised every step
+    host_in = [(s.slot_mapping.pin_memory(), s.k_new.pin_memory(), s.v_new.pin_memory(), s.q.pin_memory(),
+                s.context_lens.pin_memory()) for s in steps_in]
+    bt_host = bt_cpu.pin_memory()
+    out_host = torch.empty((S, hq, d), dtype=wl.dtype).pin_memory()
+    d_slots, d_kn, d_vn, d_q, d_ctx = (torch.empty_like(x, device=dev) for x in host_in[0])
+    d_bt = torch.empty_like(bt_cpu, device=dev)
+    h2d = sum(x.numel() * x.element_size() for x in host_in[0]) + bt_host.numel() * bt_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step(t):
+        hs, hk, hv, hq_, hc = host_in[t % wl.steps]
+        d_slots.copy_(hs, non_blocking=True)
+        d_kn.copy_(hk, non_blocking=True)
+        d_vn.copy_(hv, non_blocking=True)
+        d_q.copy_(hq_, non_blocking=True)
+        d_ctx.copy_(hc, non_blocking=True)
+        d_bt.copy_(bt_host, non_blocking=True)
+        pa.pa_append_kv(kp, vp, d_slots, d_kn, d_vn, stream=stream)
+        pa.pa_decode_attention(out, d_q, kp, vp, d_bt, d_ctx, wl.scale, max_context_len=max_ctx,
+                               partition_size=args.partition, workspace=ws, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+    for w in range(args.warmup):
+        e2e_step(w)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    te0 = time.perf_counter()
+    for k in range(args.steps):
+        e2e_step(args.warmup + k)
+    te1 = time.perf_counter()
+    e2e_s = te1 - te0
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = world * step_bytes / e2e_s / 1e9
+
+    status = pa.pa_device_status()
+    if rank != 0:
+        return
+    clocks = sampler.summary(t_busy0, t_wall1 + 0.1) if sampler else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "partition_tokens": part, "max_splits": max_splits,
+                   "l2": "inputs larger than L2: ~726 MB of K/V read per step vs 129 MB L2, no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_peak": value / peak,
+        "decode_tokens_per_s": world * S * args.steps / (total_ms * 1e-3),
+        "attention_us": 1e3 * attn_avg_ms, "append_us": 1e3 * statistics.mean(app_ms),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": measured_traffic(kv_ratio),
+                     "kernel": "pa_decode_attention (decode kernel + LSE combine), CUDA events per call",
+                     "peak_kind": f"{peak_kind} (STREAM-like copy, burst)"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks, "device_status": status,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

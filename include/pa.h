@@ -1,0 +1,204 @@
+/*
+ * pa.h -- C ABI of libpa: paged KV-cache attention for GB300 (sm_103a).
+ *
+ * The library implements the attention slice of an LLM inference engine whose
+ * KV cache is a pool of fixed 16-token blocks shared by all requests
+ * ("Mini inference engine (KV cache + sampling + quantization)", step 2 and
+ * its stretch goal; "LLM Inference Server", Optional Bonus Extensions:
+ * Paged KV-Cache Block Allocator; "LLM Inference Server From Scratch",
+ * How it works, 3 Block Manager and 4 Attention Kernel).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The library
+ *    allocates no device memory, never synchronises, and enqueues its kernels
+ *    on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *    stream).  Results are ready when the stream reaches that point.
+ *  - Pool layout, identical for K and V: [num_blocks][num_kv_heads][16][head_dim],
+ *    row-major, element type `dtype`.  Each (block, head) tile is one contiguous
+ *    16*head_dim*elem_bytes run.  Token position p of a sequence lives in
+ *    logical block p/16 at offset p%16; logical block j is physical block
+ *    block_tables[seq*max_blocks_per_seq + j].
+ *  - Grouped-query attention: q head h reads KV head h / (num_q_heads/num_kv_heads).
+ *  - context_lens[s] counts every cached token of sequence s, including the
+ *    token appended in this step (the new token is at position context_len-1).
+ *  - q, K, V and out share one dtype; scores, softmax and accumulation run in
+ *    fp32; out is rounded to the dtype once (round-to-nearest-even).
+ *  - Return value: PA_OK, or a negative code with a message in pa_last_error().
+ *    All argument checks run on the host BEFORE anything is enqueued, so a
+ *    rejected call leaves the stream and the device untouched.  Device-side
+ *    data (slots, block ids, context lengths) is range-checked in the kernels:
+ *    an out-of-range value is skipped and recorded in a device status word
+ *    (see pa_device_status), never dereferenced.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#define PA_BLOCK_SIZE 16
+#define PA_VERSION 1
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = -1,     /* bad argument (null, misaligned, inconsistent sizes) */
+  PA_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, dtype or group size  */
+  PA_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed          */
+  PA_ERR_DEVICE = -4       /* pa_device_status found a flagged device-side problem */
+};
+
+/* bits of the device status word */
+enum {
+  PA_DEV_BAD_SLOT = 1,        /* append: slot >= num_blocks*16 (row skipped)          */
+  PA_DEV_BAD_BLOCK_ID = 2,    /* a block-table entry outside [0, num_blocks) (skipped) */
+  PA_DEV_BAD_CONTEXT = 4,     /* context_len < 0 or > max_blocks_per_seq*16 (clamped) */
+  PA_DEV_WAIT_TIMEOUT = 8     /* a bounded wait on a copy barrier gave up              */
+};
+
+/* Geometry of the KV pool, shared by every call. */
+typedef struct {
+  int num_blocks;   /* physical blocks in each of k_pool and v_pool (>= 1)   */
+  int num_kv_heads; /* H_kv (>= 1)                                            */
+  int block_size;   /* tokens per block; must be PA_BLOCK_SIZE (16)          */
+  int head_dim;     /* D: 64 or 128                                           */
+  int dtype;        /* pa_dtype of pools, q, k_new/v_new and out             */
+} pa_pool_desc;
+
+/* Library version (PA_VERSION of the build). */
+PA_API int pa_version(void);
+
+/* Message for the last non-OK return on the calling thread ("" if none).
+ * The pointer stays valid until the next pa_* call on that thread. */
+PA_API const char* pa_last_error(void);
+
+/*
+ * pa_append_kv -- write this step's new K/V rows into the pool.
+ *
+ * The per-step in-place KV write ("Mini inference engine", step 2: append on
+ * each step; "LLM Inference Server", Stage 1: new K/V slices written into
+ * pre-allocated buffers in place), routed through a slot mapping into the
+ * 16-token block pool.  For every token t with slot = slot_mapping[t] >= 0:
+ *     k_pool[slot/16][h][slot%16][:] = k_new[t][h][:]   for all h,
+ * and the same for V.  A negative slot skips the token (padding).  The copy is
+ * bit-exact.  Slots must be distinct; with duplicates the surviving row is
+ * unspecified.
+ *
+ *   k_pool, v_pool : [num_blocks][H_kv][16][D], written in place
+ *   slot_mapping   : int64 [num_tokens]
+ *   k_new, v_new   : [num_tokens][H_kv][D]
+ *   num_tokens     : >= 0 (0 is a no-op)
+ * Errors: PA_ERR_INVALID for null pointers, pointers not 16-byte aligned,
+ * block_size != 16, num_tokens < 0; PA_ERR_UNSUPPORTED for other head_dim or
+ * dtype.  A slot >= num_blocks*16 is skipped and sets PA_DEV_BAD_SLOT.
+ */
+PA_API int pa_append_kv(void* k_pool, void* v_pool, const int64_t* slot_mapping,
+                 const void* k_new, const void* v_new, int num_tokens,
+                 const pa_pool_desc* pool, void* stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device scratch pa_decode_attention
+ * needs for the split-K partials of this batch shape (0 when no sequence can
+ * span more than one partition).  partition_size as in pa_decode_attention.
+ * Returns 0 and sets pa_last_error on invalid arguments.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_context_len,
+                                int partition_size, const pa_pool_desc* pool);
+
+/* The partition (tokens per split-K unit) that pa_decode_attention will use
+ * for this shape: partition_size itself when nonzero, else the automatic choice. */
+PA_API int pa_decode_partition_size(int num_seqs, int max_context_len, int partition_size,
+                             const pa_pool_desc* pool);
+
+/*
+ * pa_decode_attention -- one query token per sequence over its paged cache.
+ *
+ * For each sequence s and q head h (KV head g = h / G):
+ *     out[s][h] = softmax_i( scale * q[s][h] . K_s[i][g] ) V_s[i][g],  i < context_lens[s]
+ * where K_s / V_s are the sequence's blocks read through its block table
+ * (decode passes only the newly sampled token, "LLM Inference Server", Stage 1;
+ * the fused attention kernel with GQA of "LLM Inference Server From Scratch",
+ * How it works, 4).  A sequence with context_len 0 gets a zero row.
+ *
+ * Work is split into partitions of `partition_size` tokens (split-K); a
+ * sequence spanning several partitions has its partial softmax results merged
+ * by log-sum-exp in a second kernel.  The result does not depend on the
+ * partition beyond fp32 rounding.
+ *
+ *   out               : [num_seqs][num_q_heads][D], written
+ *   q                 : [num_seqs][num_q_heads][D]
+ *   k_pool, v_pool    : pool layout above, read only
+ *   block_tables      : int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens      : int32 [num_seqs], each in [0, max_context_len]
+ *   scale             : softmax scale (e.g. 1/sqrt(D)), finite
+ *   max_context_len   : host-known upper bound of context_lens (sizes the grid;
+ *                       no device-to-host copy is made)
+ *   partition_size    : tokens per split-K unit: 0 = automatic, else a multiple
+ *                       of 16 in [16, 2048]
+ *   workspace         : device scratch of >= pa_decode_workspace_size(...) bytes,
+ *                       16-byte aligned (may be NULL when that size is 0).  Its
+ *                       contents need no initialisation; two calls in flight at
+ *                       once must not share it.
+ * Errors: PA_ERR_INVALID for null or misaligned pointers, num_q_heads not a
+ * multiple of num_kv_heads, max_context_len > max_blocks_per_seq*16, a bad
+ * partition_size, a too-small workspace or a non-finite scale;
+ * PA_ERR_UNSUPPORTED for head_dim not 64/128, G > 8, or a pool too large for
+ * 32-bit row coordinates.
+ */
+PA_API int pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        float scale, int num_seqs, int num_q_heads, int max_blocks_per_seq,
+                        int max_context_len, int partition_size, const pa_pool_desc* pool,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_prefill_attention -- the causal prompt pass over the same pool.
+ *
+ * Prefill processes all prompt tokens at once (q_len = prompt length,
+ * "LLM Inference Server", Stage 1) under a causal mask ("LLM Inference Server
+ * From Scratch", What you build / How it works, 4).  Sequence s owns query
+ * rows cu_q_lens[s] .. cu_q_lens[s+1]-1; its K/V (prompt tokens already
+ * appended) are the first context_lens[s] positions of its blocks.  Query i of
+ * the sequence sits at position p = context_lens[s] - q_len_s + i and attends
+ * keys 0..p, so a cached prefix (context_len > q_len) is handled too.
+ *
+ *   out, q        : [cu_q_lens[num_seqs]][num_q_heads][D]
+ *   block_tables  : int32 [num_seqs][max_blocks_per_seq]
+ *   cu_q_lens     : int32 [num_seqs+1], non-decreasing, cu_q_lens[0] = 0
+ *   context_lens  : int32 [num_seqs], context_lens[s] >= q_len_s
+ *   max_q_len     : host-known max of q_len_s (sizes the grid)
+ *   max_context_len : host-known max of context_lens (<= max_blocks_per_seq*16)
+ * Errors as pa_decode_attention; fp32 pools are PA_ERR_UNSUPPORTED here (the
+ * prompt pass runs on bf16/fp16 tensor cores).
+ */
+PA_API int pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, const int32_t* cu_q_lens,
+                         const int32_t* context_lens, float scale, int num_seqs,
+                         int num_q_heads, int max_blocks_per_seq, int max_q_len,
+                         int max_context_len, const pa_pool_desc* pool, void* stream);
+
+/*
+ * pa_device_status -- read and clear the device status word of the current
+ * device (bits PA_DEV_*).  Synchronises `stream` first.  Returns PA_OK when the
+ * word was 0, PA_ERR_DEVICE when any bit was set (the bits are stored in
+ * *status), PA_ERR_CUDA if the read failed.
+ */
+PA_API int pa_device_status(int* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

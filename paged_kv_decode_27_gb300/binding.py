@@ -1,0 +1,215 @@
+"""Python binding of libpa (``include/pa.h``): argument marshalling only.
+
+Each function has the name of the C entry point it calls and takes torch
+tensors already on the GPU.  It checks shapes, dtypes and contiguity, passes
+raw device pointers and the current CUDA stream, and raises ``PaError`` on a
+non-OK status.  Every step of the computation runs in the CUDA library; there
+is no fallback: if ``lib/libpa.so`` has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libpa.so")
+
+PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = 0, -1, -2, -3, -4
+PA_DEV_BAD_SLOT, PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_CONTEXT, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
+BLOCK_SIZE = 16
+
+_DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
+
+
+class PaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libpa error {code}: {msg}")
+        self.code = code
+
+
+class pa_pool_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpa.so once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    pdesc = ctypes.POINTER(pa_pool_desc)
+    L.pa_version.restype = i32
+    L.pa_version.argtypes = []
+    L.pa_last_error.restype = ctypes.c_char_p
+    L.pa_last_error.argtypes = []
+    L.pa_append_kv.restype = i32
+    L.pa_append_kv.argtypes = [vp, vp, vp, vp, vp, i32, pdesc, vp]
+    L.pa_decode_workspace_size.restype = sz
+    L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, pdesc]
+    L.pa_decode_partition_size.restype = i32
+    L.pa_decode_partition_size.argtypes = [i32, i32, i32, pdesc]
+    L.pa_decode_attention.restype = i32
+    L.pa_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, pdesc,
+                                      vp, sz, vp]
+    L.pa_prefill_attention.restype = i32
+    L.pa_prefill_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32,
+                                       pdesc, vp]
+    L.pa_device_status.restype = i32
+    L.pa_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+    _lib = L
+    return L
+
+
+def pa_last_error() -> str:
+    return load_library().pa_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != PA_OK:
+        raise PaError(rc, pa_last_error())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def pool_desc(k_pool: torch.Tensor) -> pa_pool_desc:
+    """Geometry of a pool tensor laid out [num_blocks][H_kv][16][D]."""
+    if k_pool.dim() != 4 or k_pool.shape[2] != BLOCK_SIZE:
+        raise ValueError(f"pool must be [num_blocks][H_kv][16][D], got {tuple(k_pool.shape)}")
+    if k_pool.dtype not in _DTYPES:
+        raise ValueError(f"unsupported pool dtype {k_pool.dtype}")
+    n, h, b, d = k_pool.shape
+    return pa_pool_desc(int(n), int(h), int(b), int(d), _DTYPES[k_pool.dtype])
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(name: str, t: torch.Tensor):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _pools(k_pool, v_pool):
+    _cuda_contig("k_pool", k_pool)
+    _cuda_contig("v_pool", v_pool)
+    _need(k_pool.shape == v_pool.shape and k_pool.dtype == v_pool.dtype,
+          "k_pool and v_pool must have the same shape and dtype")
+    return pool_desc(k_pool)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def pa_append_kv(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Write k_new/v_new [T][H_kv][D] into the pools at slot_mapping (int64 [T])."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("slot_mapping", slot_mapping), ("k_new", k_new), ("v_new", v_new)):
+        _cuda_contig(n, t)
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.dim() == 1, "slot_mapping must be int64 [T]")
+    T = slot_mapping.shape[0]
+    shape = (T, k_pool.shape[1], k_pool.shape[3])
+    _need(tuple(k_new.shape) == shape and tuple(v_new.shape) == shape, f"k_new/v_new must be {shape}")
+    _need(k_new.dtype == k_pool.dtype and v_new.dtype == k_pool.dtype, "k_new/v_new dtype must match the pool")
+    L = load_library()
+    _check(L.pa_append_kv(_ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping), _ptr(k_new), _ptr(v_new),
+                          int(T), ctypes.byref(desc), _stream(stream)))
+
+
+def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, max_context_len: int,
+                             k_pool: torch.Tensor, partition_size: int = 0) -> int:
+    L = load_library()
+    desc = pool_desc(k_pool)
+    n = L.pa_decode_workspace_size(int(num_seqs), int(num_q_heads), int(max_context_len),
+                                   int(partition_size), ctypes.byref(desc))
+    msg = pa_last_error()
+    if msg:
+        raise PaError(PA_ERR_INVALID, msg)
+    return int(n)
+
+
+def pa_decode_partition_size(num_seqs: int, max_context_len: int, k_pool: torch.Tensor,
+                             partition_size: int = 0) -> int:
+    L = load_library()
+    desc = pool_desc(k_pool)
+    return int(L.pa_decode_partition_size(int(num_seqs), int(max_context_len), int(partition_size),
+                                          ctypes.byref(desc)))
+
+
+def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                        block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                        max_context_len: int, partition_size: int = 0,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """out, q: [S][H_q][D]; block_tables int32 [S][max_blocks]; context_lens int32 [S].
+    ``workspace`` (uint8 CUDA tensor) is allocated here when not given."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 3 and q.shape[2] == k_pool.shape[3], "q must be [S][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype == k_pool.dtype, "out/q shape or dtype mismatch")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
+    L = load_library()
+    need = pa_decode_workspace_size(S, hq, max_context_len, k_pool, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.pa_decode_attention(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                 _ptr(context_lens), float(scale), S, hq, int(block_tables.shape[1]),
+                                 int(max_context_len), int(partition_size), ctypes.byref(desc),
+                                 _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                         block_tables: torch.Tensor, cu_q_lens: torch.Tensor, context_lens: torch.Tensor,
+                         scale: float, max_q_len: int, max_context_len: int, stream=None) -> None:
+    """out, q: [sum q_len][H_q][D]; cu_q_lens int32 [S+1]; context_lens int32 [S]."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("cu_q_lens", cu_q_lens),
+                 ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 3 and q.shape[2] == k_pool.shape[3], "q must be [sum q_len][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype == k_pool.dtype, "out/q shape or dtype mismatch")
+    S = int(context_lens.shape[0])
+    _need(cu_q_lens.dtype == torch.int32 and tuple(cu_q_lens.shape) == (S + 1,), "cu_q_lens must be int32 [S+1]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    L = load_library()
+    _check(L.pa_prefill_attention(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                  _ptr(cu_q_lens), _ptr(context_lens), float(scale), S, int(q.shape[1]),
+                                  int(block_tables.shape[1]), int(max_q_len), int(max_context_len),
+                                  ctypes.byref(desc), _stream(stream)))
+
+
+def pa_device_status(stream=None) -> int:
+    """Read and clear the device status word (PA_DEV_* bits); 0 when clean."""
+    L = load_library()
+    st = ctypes.c_int(0)
+    rc = L.pa_device_status(ctypes.byref(st), _stream(stream))
+    if rc not in (PA_OK, PA_ERR_DEVICE):
+        raise PaError(rc, pa_last_error())
+    return int(st.value)

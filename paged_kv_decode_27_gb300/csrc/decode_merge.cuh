@@ -1,0 +1,73 @@
+// decode_merge.cuh -- merge the per-warp online-softmax states of one CTA and
+// store either the final output (single partition) or one split-K partial.
+//
+// Each warp leaves, for every query head h of the group (h < G <= 8):
+//   red_m[w][h]  running max of the log2-domain scores,
+//   red_l[w][h]  sum of 2^(x - m) over the warp's tokens,
+//   red_o[w][h][d] sum of 2^(x - m) * v[d].
+// A warp that saw no token has m = -inf, l = 0, o = 0 and weighs nothing.
+#pragma once
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <typename T, int W, int D>
+__device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float* red_o,
+                                                const float* red_m, const float* red_l, int G,
+                                                int s, int kvh, int split, int n_splits) {
+  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float mw = red_m[w * 8 + h];
+        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        L += f * red_l[w * 8 + h];
+        O += f * red_o[(w * 8 + h) * D + d];
+      }
+    }
+    const int hq = kvh * G + h;
+    const float o = (L > 0.f) ? O / L : 0.f;
+    if (n_splits == 1) {
+      T* out = static_cast<T*>(a.out);
+      out[(static_cast<size_t>(s) * a.num_q_heads + hq) * D + d] = Elem<T>::from_f(o);
+    } else {
+      const size_t row = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.max_splits + split;
+      a.ws_o[row * D + d] = o;
+      if (d == 0) a.ws_lse[row] = (L > 0.f) ? M + log2f(L) : -INFINITY;
+    }
+  }
+}
+
+// A sequence with an empty context produces zero rows for its heads.
+template <typename T, int D>
+__device__ __forceinline__ void store_zero_rows(const DecodeArgs& a, int G, int s, int kvh,
+                                                int nthreads) {
+  T* out = static_cast<T*>(a.out);
+  for (int idx = threadIdx.x; idx < G * D; idx += nthreads) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    out[(static_cast<size_t>(s) * a.num_q_heads + kvh * G + h) * D + d] = Elem<T>::from_f(0.f);
+  }
+}
+
+// Context length as the kernels use it: clamped to what the block table can
+// address, with the clamp recorded in the status word.
+__device__ __forceinline__ int checked_context(const DecodeArgs& a, int s, bool report) {
+  int c = __ldg(a.context_lens + s);
+  const int cap = min(a.max_blocks_per_seq * kBlock, a.max_context_len);
+  if (c < 0 || c > cap) {
+    if (report) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+    c = c < 0 ? 0 : cap;
+  }
+  return c;
+}
+
+}  // namespace pa

@@ -1,0 +1,388 @@
+// pa_api.cu -- the C ABI of libpa (declared in include/pa.h).
+//
+// Host side only: argument checks (all before anything is enqueued, so a bad
+// call never reaches the GPU -- the idea of rejecting invalid requests before
+// touching the GPU, "LLM Inference Server", Stage 4 input validation), the
+// split-K partition choice, TMA descriptors for the KV pool, and the kernel
+// launches.  No allocation, no synchronisation.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+// Device status word (PA_DEV_* bits), one per device that loads the library.
+__device__ int g_pa_status = 0;
+
+namespace {
+
+constexpr int kGb300Sms = 152;
+// Split-K partitions are shrunk until a batch yields at least this many
+// (sequence, KV head, partition) units, i.e. several CTAs per SM.
+constexpr long long kTargetUnits = 4LL * kGb300Sms;
+constexpr int kMaxPartition = 2048;   // 32 blocks per warp of a 4-warp CTA
+
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dtype) {
+  switch (dtype) {
+    case PA_F32: return 4;
+    case PA_BF16:
+    case PA_F16: return 2;
+    default: return 0;
+  }
+}
+
+int check_pool(const pa_pool_desc* pool) {
+  if (!pool) return fail(PA_ERR_INVALID, "pool descriptor is NULL");
+  if (pool->block_size != PA_BLOCK_SIZE)
+    return fail(PA_ERR_INVALID, "block_size must be %d (got %d)", PA_BLOCK_SIZE, pool->block_size);
+  if (pool->num_blocks < 1) return fail(PA_ERR_INVALID, "num_blocks must be >= 1");
+  if (pool->num_kv_heads < 1) return fail(PA_ERR_INVALID, "num_kv_heads must be >= 1");
+  if (elem_bytes(pool->dtype) == 0) return fail(PA_ERR_UNSUPPORTED, "dtype %d not supported", pool->dtype);
+  if (pool->head_dim != 64 && pool->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", pool->head_dim);
+  if (static_cast<long long>(pool->num_blocks) * pool->num_kv_heads * PA_BLOCK_SIZE > 0x7fffffffLL)
+    return fail(PA_ERR_UNSUPPORTED, "pool too large for 32-bit row coordinates");
+  return PA_OK;
+}
+
+int* status_ptr() {
+  static std::mutex mu;
+  static int* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+int choose_partition(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
+  if (requested > 0) return requested;
+  int p = 512;
+  while (p > 64) {
+    const long long units =
+        static_cast<long long>(num_seqs) * num_kv_heads * ((max_context_len + p - 1) / p);
+    if (units >= kTargetUnits) break;
+    p /= 2;
+  }
+  return p;
+}
+
+int max_splits_for(int max_context_len, int part_blocks) {
+  const int nblk = (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  return nblk == 0 ? 1 : (nblk + part_blocks - 1) / part_blocks;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t o_bytes, lse_off, total;
+};
+
+WsLayout ws_layout(int num_seqs, int num_q_heads, int max_splits, int head_dim) {
+  WsLayout w{0, 0, 0};
+  if (max_splits <= 1) return w;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_splits;
+  w.o_bytes = rows * head_dim * sizeof(float);
+  w.lse_off = align256(w.o_bytes);
+  w.total = w.lse_off + rows * sizeof(float);
+  return w;
+}
+
+// ---- TMA descriptors of the pool ---------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// The pool viewed as a 2-D tensor of rows (block, head, offset) x head_dim,
+// loaded in boxes of 16 rows x 64 elements (128 bytes) with 128-byte swizzle.
+int make_pool_map(CUtensorMap* map, const void* pool_ptr, const pa_pool_desc* pool) {
+  auto enc = encode_fn();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapDataType dt =
+      pool->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(pool->head_dim),
+                        static_cast<cuuint64_t>(pool->num_blocks) * pool->num_kv_heads * PA_BLOCK_SIZE};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pool->head_dim) * 2};
+  cuuint32_t box[2] = {64, PA_BLOCK_SIZE};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(pool_ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return PA_OK;
+}
+
+// Small per-thread cache: encoding is cheap but not free, and the same pools
+// are passed on every step.
+struct MapEntry {
+  const void* ptr;
+  pa_pool_desc desc;
+  CUtensorMap map;
+  bool used;
+};
+
+int pool_map(CUtensorMap* out, const void* ptr, const pa_pool_desc* pool) {
+  thread_local MapEntry cache[8] = {};
+  thread_local int next = 0;
+  for (auto& e : cache) {
+    if (e.used && e.ptr == ptr && std::memcmp(&e.desc, pool, sizeof(pa_pool_desc)) == 0) {
+      *out = e.map;
+      return PA_OK;
+    }
+  }
+  MapEntry& e = cache[next];
+  next = (next + 1) % 8;
+  const int rc = make_pool_map(&e.map, ptr, pool);
+  if (rc != PA_OK) {
+    e.used = false;
+    return rc;
+  }
+  e.ptr = ptr;
+  e.desc = *pool;
+  e.used = true;
+  *out = e.map;
+  return PA_OK;
+}
+
+int check_decode_shape(int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_context_len,
+                       int partition_size, const pa_pool_desc* pool) {
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs must be >= 0");
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs > 65535");
+  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                num_q_heads, pool->num_kv_heads);
+  if (num_q_heads / pool->num_kv_heads > 8)
+    return fail(PA_ERR_UNSUPPORTED, "query group size %d > 8", num_q_heads / pool->num_kv_heads);
+  if (pool->num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  if (max_context_len < 0) return fail(PA_ERR_INVALID, "max_context_len must be >= 0");
+  if (max_blocks_per_seq < 0) return fail(PA_ERR_INVALID, "max_blocks_per_seq must be >= 0");
+  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks_per_seq) * PA_BLOCK_SIZE)
+    return fail(PA_ERR_INVALID, "max_context_len %d exceeds max_blocks_per_seq*16 = %lld", max_context_len,
+                static_cast<long long>(max_blocks_per_seq) * PA_BLOCK_SIZE);
+  if (partition_size != 0 &&
+      (partition_size < PA_BLOCK_SIZE || partition_size > kMaxPartition || partition_size % PA_BLOCK_SIZE))
+    return fail(PA_ERR_INVALID, "partition_size %d must be 0 or a multiple of 16 in [16, %d]", partition_size,
+                kMaxPartition);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return PA_VERSION; }
+
+const char* pa_last_error(void) { return t_err.c_str(); }
+
+int pa_append_kv(void* k_pool, void* v_pool, const int64_t* slot_mapping, const void* k_new,
+                 const void* v_new, int num_tokens, const pa_pool_desc* pool, void* stream) {
+  t_err.clear();
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens must be >= 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!k_pool || !v_pool || !slot_mapping || !k_new || !v_new)
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(PA_ERR_INVALID, "pools and k_new/v_new must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+    return fail(PA_ERR_INVALID, "slot_mapping must be 8-byte aligned");
+  const int row_bytes = pool->head_dim * elem_bytes(pool->dtype);
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  cudaError_t e = pa::launch_append(k_pool, v_pool, slot_mapping, k_new, v_new, num_tokens,
+                                    pool->num_kv_heads, row_bytes, pool->num_blocks, status,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append_kv launch");
+  return PA_OK;
+}
+
+int pa_decode_partition_size(int num_seqs, int max_context_len, int partition_size,
+                             const pa_pool_desc* pool) {
+  t_err.clear();
+  if (check_pool(pool) != PA_OK) return 0;
+  return choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_context_len, int partition_size,
+                                const pa_pool_desc* pool) {
+  t_err.clear();
+  const int mb = (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  if (check_decode_shape(num_seqs, num_q_heads, mb, max_context_len, partition_size, pool) != PA_OK) return 0;
+  const int p = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int ms = max_splits_for(max_context_len, p / PA_BLOCK_SIZE);
+  return ws_layout(num_seqs, num_q_heads, ms, pool->head_dim).total;
+}
+
+int pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_context_len,
+                        int partition_size, const pa_pool_desc* pool, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool);
+  if (rc != PA_OK) return rc;
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_pool || !v_pool || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(PA_ERR_INVALID, "out, q and the pools must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "block_tables and context_lens must be 4-byte aligned");
+
+  const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int part_blocks = part / PA_BLOCK_SIZE;
+  const int max_splits = max_splits_for(max_context_len, part_blocks);
+  const WsLayout ws = ws_layout(num_seqs, num_q_heads, max_splits, pool->head_dim);
+  if (ws.total > 0) {
+    if (!workspace) return fail(PA_ERR_INVALID, "workspace of %zu bytes required, got NULL", ws.total);
+    if (workspace_bytes < ws.total)
+      return fail(PA_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, ws.total);
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+  }
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+
+  pa::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.head_dim = pool->head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.num_blocks = pool->num_blocks;
+  a.part_blocks = part_blocks;
+  a.max_splits = max_splits;
+  a.ws_o = ws.total ? static_cast<float*>(workspace) : nullptr;
+  a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
+  a.status = status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e;
+  if (pool->dtype == PA_F32) {
+    e = pa::launch_decode_simt(a, pool->dtype, st);
+  } else {
+    CUtensorMap kmap, vmap;
+    if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
+    if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
+    e = pa::launch_decode_tc(a, pool->dtype, kmap, vmap, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (max_splits > 1) {
+    e = pa::launch_combine(a, pool->dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return PA_OK;
+}
+
+int pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, const int32_t* cu_q_lens, const int32_t* context_lens,
+                         float scale, int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_q_len,
+                         int max_context_len, const pa_pool_desc* pool, void* stream) {
+  t_err.clear();
+  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, 0, pool);
+  if (rc != PA_OK) return rc;
+  if (pool->dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "prefill needs bf16 or fp16 pools");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
+  if (max_q_len < 0 || max_q_len > max_context_len)
+    return fail(PA_ERR_INVALID, "max_q_len %d must be in [0, max_context_len=%d]", max_q_len, max_context_len);
+  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (!out || !q || !k_pool || !v_pool || !block_tables || !cu_q_lens || !context_lens)
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(PA_ERR_INVALID, "out, q and the pools must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if ((max_q_len + 63) / 64 > 0x7fffffff) return fail(PA_ERR_UNSUPPORTED, "max_q_len too large");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+
+  pa::PrefillArgs a{};
+  a.out = out;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.cu_q_lens = cu_q_lens;
+  a.context_lens = context_lens;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.head_dim = pool->head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = pool->num_blocks;
+  a.max_q_len = max_q_len;
+  a.status = status;
+  CUtensorMap kmap, vmap;
+  if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
+  if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
+  cudaError_t e = pa::launch_prefill_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return PA_OK;
+}
+
+int pa_device_status(int* status, void* stream) {
+  t_err.clear();
+  if (!status) return fail(PA_ERR_INVALID, "status pointer is NULL");
+  int* dev = status_ptr();
+  if (!dev) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, dev, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  *status = host;
+  if (host != 0) return fail(PA_ERR_DEVICE, "device status word 0x%x", host);
+  return PA_OK;
+}
+
+}  // extern "C"

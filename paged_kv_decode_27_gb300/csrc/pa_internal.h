@@ -1,0 +1,71 @@
+// pa_internal.h -- launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Everything a decode launch needs; passed to the kernels by value.
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float scale_log2;        // softmax scale * log2(e): scores live in the log2 domain
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int max_blocks_per_seq;
+  int max_context_len;     // host-known bound; larger device values are clamped
+  int num_blocks;
+  int part_blocks;         // pool blocks per split-K partition
+  int max_splits;          // ceil(ceil(max_context_len / 16) / part_blocks)
+  float* ws_o;             // [S][H_q][max_splits][D]  normalised partial outputs
+  float* ws_lse;           // [S][H_q][max_splits]     partial log2-sum-exp2
+  int* status;             // device status word (PA_DEV_* bits)
+};
+
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* cu_q_lens;
+  const int32_t* context_lens;
+  float scale_log2;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int max_q_len;
+  int* status;
+};
+
+cudaError_t launch_append(void* k_pool, void* v_pool, const int64_t* slot_mapping,
+                          const void* k_new, const void* v_new, int num_tokens,
+                          int num_kv_heads, int row_bytes, int num_blocks, int* status,
+                          cudaStream_t stream);
+
+// Tensor-core decode (bf16/fp16 pools, D in {64, 128}, G <= 8).
+cudaError_t launch_decode_tc(const DecodeArgs& a, int dtype, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, cudaStream_t stream);
+
+// CUDA-core decode (any supported dtype; the fp32 path).
+cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t stream);
+
+// Log-sum-exp merge of the split-K partials into out.
+cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t stream);
+
+// Tensor-core causal prefill (bf16/fp16 pools, D in {64, 128}).
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, cudaStream_t stream);
+
+}  // namespace pa

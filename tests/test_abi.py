@@ -1,0 +1,133 @@
+"""The C-ABI library on the CPU host: it loads, exports every symbol that
+include/pa.h declares, and rejects bad arguments on the host before touching
+any GPU (no compute calls here)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_decode_27_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_27_gb300 import build
+    build.build()
+    return B.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for want in ("pa_append_kv", "pa_decode_attention", "pa_prefill_attention", "pa_decode_workspace_size",
+                 "pa_last_error", "pa_device_status", "pa_version"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version(lib):
+    assert lib.pa_version() == 1
+
+
+def _desc(nb=64, hkv=8, bs=16, d=128, dt=B.PA_BF16):
+    return B.pa_pool_desc(nb, hkv, bs, d, dt)
+
+
+FAKE = 0x10000000   # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def _decode(lib, desc, out=FAKE, q=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, cl=FAKE, scale=0.125, S=4, hq=32, mb=8,
+            maxc=100, part=0, ws=None, wsb=0):
+    return lib.pa_decode_attention(ctypes.c_void_p(out), ctypes.c_void_p(q), ctypes.c_void_p(kp),
+                                   ctypes.c_void_p(vp), ctypes.c_void_p(bt), ctypes.c_void_p(cl), scale, S, hq,
+                                   mb, maxc, part, ctypes.byref(desc), ctypes.c_void_p(ws), wsb, None)
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    d = _desc()
+    assert _decode(lib, d, out=0) == B.PA_ERR_INVALID
+    assert "null" in B.pa_last_error()
+    assert _decode(lib, _desc(bs=32)) == B.PA_ERR_INVALID
+    assert _decode(lib, _desc(d=96)) == B.PA_ERR_UNSUPPORTED
+    assert _decode(lib, _desc(dt=7)) == B.PA_ERR_UNSUPPORTED
+    assert _decode(lib, d, hq=12) == B.PA_ERR_INVALID              # 12 % 8 != 0
+    assert _decode(lib, d, hq=8 * 16) == B.PA_ERR_UNSUPPORTED       # group of 16
+    assert _decode(lib, d, q=FAKE + 8) == B.PA_ERR_INVALID          # misaligned
+    assert _decode(lib, d, maxc=8 * 16 + 1) == B.PA_ERR_INVALID     # exceeds block table
+    assert _decode(lib, d, part=17) == B.PA_ERR_INVALID
+    assert _decode(lib, d, part=4096) == B.PA_ERR_INVALID
+    assert _decode(lib, d, scale=float("nan")) == B.PA_ERR_INVALID
+    assert _decode(lib, d, S=-1) == B.PA_ERR_INVALID
+    # a split-K shape without workspace, then with a too-small one
+    assert _decode(lib, d, maxc=128, part=16) == B.PA_ERR_INVALID
+    assert "workspace" in B.pa_last_error()
+    assert _decode(lib, d, maxc=128, part=16, ws=FAKE, wsb=16) == B.PA_ERR_INVALID
+    assert _decode(lib, _desc(nb=1 << 25)) == B.PA_ERR_UNSUPPORTED  # rows overflow int32
+
+
+def test_zero_sequences_is_a_no_op(lib):
+    assert _decode(lib, _desc(), S=0) == B.PA_OK
+
+
+def test_append_rejects_bad_arguments_on_the_host(lib):
+    d = _desc()
+    f = ctypes.c_void_p(FAKE)
+    call = lambda kp=f, slots=f, T=4, desc=d: lib.pa_append_kv(kp, f, slots, f, f, T, ctypes.byref(desc), None)
+    assert call(kp=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
+    assert call(kp=ctypes.c_void_p(FAKE + 4)) == B.PA_ERR_INVALID
+    assert call(slots=ctypes.c_void_p(FAKE + 4)) == B.PA_ERR_INVALID
+    assert call(T=-1) == B.PA_ERR_INVALID
+    assert call(desc=_desc(d=80)) == B.PA_ERR_UNSUPPORTED
+    assert call(T=0) == B.PA_OK
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(lib):
+    f = ctypes.c_void_p(FAKE)
+    call = lambda desc, maxq=64, maxc=64, out=f: lib.pa_prefill_attention(
+        out, f, f, f, f, f, f, 0.1, 2, 32, 4, maxq, maxc, ctypes.byref(desc), None)
+    assert call(_desc(dt=B.PA_F32)) == B.PA_ERR_UNSUPPORTED
+    assert call(_desc(), maxq=65) == B.PA_ERR_INVALID
+    assert call(_desc(), maxc=65) == B.PA_ERR_INVALID
+    assert call(_desc(), out=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
+
+
+def test_workspace_size_and_partition(lib):
+    d = _desc(d=128)
+    # batch 64, 8 KV heads, contexts to 8224: 512-token partitions, 17 splits
+    assert lib.pa_decode_partition_size(64, 8224, 0, ctypes.byref(d)) == 512
+    n = lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(d))
+    rows = 64 * 32 * 17
+    o = rows * 128 * 4
+    assert n == ((o + 255) // 256) * 256 + rows * 4
+    # few units: the partition shrinks (8 sequences of <= 2063 tokens -> 128)
+    assert lib.pa_decode_partition_size(8, 2063, 0, ctypes.byref(_desc(d=64))) == 128
+    # one partition covers everything: no workspace
+    assert lib.pa_decode_workspace_size(4, 32, 512, 512, ctypes.byref(d)) == 0
+    assert lib.pa_decode_partition_size(4, 512, 256, ctypes.byref(d)) == 256
+
+
+def test_no_gpu_means_cuda_error_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _decode(lib, _desc(), maxc=100, mb=8, part=512) == B.PA_ERR_CUDA
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        B.load_library(str(tmp_path / "nope.so"))

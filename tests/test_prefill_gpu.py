@@ -1,0 +1,85 @@
+"""pa_prefill_attention (causal prompt pass over the pool) against the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_27_gb300 import binding as pa
+from paged_kv_decode_27_gb300 import workloads as W
+from _gpu import DEV, fill_unused_with_nan, oracle_append, run_append, run_decode
+from _util import assert_close_to_ref, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_prefill(wl, q, cu, ctx, kp, vp, bt):
+    out = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    qlens = (cu[1:] - cu[:-1])
+    pa.pa_prefill_attention(out, q.to(DEV), kp, vp, bt.contiguous().to(DEV), cu.to(DEV), ctx.to(DEV), wl.scale,
+                            max_q_len=int(qlens.max()), max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    return out
+
+
+def _case(seed, qlens, prior, hq=32, hkv=8, d=128, dtype=torch.bfloat16):
+    ctx = [a + b for a, b in zip(qlens, prior)]
+    wl = W.small_random(seed, len(ctx), 0, hq, hkv, d, dtype, ctx=ctx)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn((sum(qlens), hq, d), generator=g).to(dtype)
+    cu = torch.tensor([0] + list(np.cumsum(qlens)), dtype=torch.int32)
+    return wl, q, cu, torch.tensor(ctx, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("qlens,prior", [
+    ([1, 15, 16, 17, 63, 64, 65, 130], [0] * 8),
+    ([5, 64, 100], [40, 3, 200]),          # cached prefix before the prompt
+    ([257], [0]),
+])
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(32, 8, 128, torch.bfloat16), (8, 8, 64, torch.bfloat16),
+                                            (16, 2, 64, torch.float16)])
+def test_prefill_small(qlens, prior, hq, hkv, d, dtype):
+    wl, q, cu, ctx = _case(50 + sum(qlens) + d, qlens, prior, hq, hkv, d, dtype)
+    fill_unused_with_nan(wl, ctx)
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    out = _run_prefill(wl, q, cu, ctx, kp, vp, wl.block_tables)
+    ref = oracle.prefill_ref(to_np(q), to_np(wl.k_pool), to_np(wl.v_pool), wl.block_tables.numpy(), cu.numpy(),
+                             ctx.numpy(), wl.scale)
+    assert_close_to_ref(out, ref, dtype, "prefill")
+    assert pa.pa_device_status() == 0
+
+
+def test_prefill_rows_match_gpu_decode():
+    """Row i of the prompt pass and a decode of the same query at context
+    position+1 agree (both GPU paths, within the bf16 bar of each other)."""
+    wl, q, cu, ctx = _case(60, [200], [0])
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    out = _run_prefill(wl, q, cu, ctx, kp, vp, wl.block_tables)
+    for i in (0, 15, 16, 63, 64, 199):
+        st = W.StepInputs(slot_mapping=torch.full((1,), -1, dtype=torch.int64),
+                          k_new=torch.empty((1, 8, 128), dtype=torch.bfloat16),
+                          v_new=torch.empty((1, 8, 128), dtype=torch.bfloat16),
+                          q=q[i:i + 1].clone(), context_lens=torch.tensor([i + 1], dtype=torch.int32))
+        dec = run_decode(wl, st, kp, vp)
+        assert torch.max(torch.abs(dec[0].float() - out[i].float())).item() < 2e-2
+
+
+def test_mixed_mistral7b_prefill_sampled_rows():
+    """The four prompts (512..2048) of the mixed continuous-batching step in the
+    benchmark's launch configuration; oracle on sampled rows of every prompt
+    (first rows, block and tile boundaries, last rows)."""
+    wl = W.mixed_mistral7b()
+    st = wl.step(0)
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    run_append(wl, st, kp, vp)
+    k_np, v_np = oracle_append(wl, st)
+    out = _run_prefill(wl, st.q_prefill, st.cu_q_lens, st.prefill_context_lens, kp, vp, wl.prefill_block_tables)
+    rows = []
+    for s, L in enumerate(wl.prompt_lens):
+        base = int(st.cu_q_lens[s])
+        rows += [base + i for i in (0, 1, 15, 16, 63, 64, 65, L // 2, L - 2, L - 1)]
+    ref = oracle.prefill_ref(to_np(st.q_prefill), k_np, v_np, wl.prefill_block_tables.numpy(),
+                             st.cu_q_lens.numpy(), st.prefill_context_lens.numpy(), wl.scale, rows=rows)
+    assert_close_to_ref(out[rows], ref[rows], wl.dtype, "mixed prefill")
+    assert pa.pa_device_status() == 0
