@@ -48,6 +48,11 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--partition", type=int, default=0)
+    p.add_argument("--workload", default=WORKLOAD,
+                   help="llama3_8b_decode (the headline line) or one of tiny_fp32, llama32_1b_decode, "
+                        "prefix_shared_8k, mixed_mistral7b (per-call figures for that workload)")
+    p.add_argument("--quick", action="store_true",
+                   help="no CPU baseline, no 1 s pre-warm, no end-to-end pass (for profiler runs)")
     return p.parse_args()
 
 
@@ -142,9 +147,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(win)}
 
 
-def cpu_baseline(max_seconds: float = 20.0):
-    """Time the float64 CPU oracle on a bounded sample of the workload (step 0,
-    sequences in order until max_seconds), in a fresh 1-thread process."""
+def cpu_baseline(max_seconds: float = 10.0):
+    """Time the float64 CPU oracle on a bounded sample of the workload: whole
+    decode steps (all 64 sequences, all heads) in order, each after its append,
+    until max_seconds of decode time; in a fresh 1-thread process."""
     code = r"""
 import json, os, sys, time
 sys.path.insert(0, %r)
@@ -153,32 +159,36 @@ torch.set_num_threads(1)
 import oracle
 from paged_kv_decode_27_gb300 import workloads as W
 wl = W.%s()
-st = wl.step(0)
 def npv(t):
     t = t.contiguous()
     return t.view(torch.int16).numpy().view('uint16') if t.dtype == torch.bfloat16 else t.numpy()
-kp, vp = oracle.append_ref(npv(wl.k_pool), npv(wl.v_pool), st.slot_mapping.numpy(), npv(st.k_new), npv(st.v_new))
-bt = wl.decode_block_tables.contiguous().numpy(); ctx = st.context_lens.numpy(); q = npv(st.q)
-done = []; t0 = time.perf_counter()
-for s in range(len(ctx)):
-    oracle.decode_ref(q, kp, vp, bt, ctx, wl.scale, seqs=[s])
-    done.append(s)
-    if time.perf_counter() - t0 > %f: break
-el = time.perf_counter() - t0
+kp, vp = npv(wl.k_pool), npv(wl.v_pool)
+bt = wl.decode_block_tables.contiguous().numpy()
+el = 0.0; b = 0; tok = 0; steps = 0
 e = 2; hkv, d, hq = wl.num_kv_heads, wl.head_dim, wl.num_q_heads
-b = sum(int(ctx[s]) * 2 * hkv * d * e + 2 * hq * d * e + 4 * ((int(ctx[s]) + 15) // 16) + 4 for s in done)
-print(json.dumps({"seconds": el, "seqs": len(done), "bytes": b, "tokens": sum(int(ctx[s]) for s in done)}))
+for t in range(wl.steps):
+    st = wl.step(t)
+    kp, vp = oracle.append_ref(kp, vp, st.slot_mapping.numpy(), npv(st.k_new), npv(st.v_new))
+    ctx = st.context_lens.numpy()
+    t0 = time.perf_counter()
+    oracle.decode_ref(npv(st.q), kp, vp, bt, ctx, wl.scale)
+    el += time.perf_counter() - t0
+    b += sum(int(c) * 2 * hkv * d * e + 2 * hq * d * e + 4 * ((int(c) + 15) // 16) + 4 for c in ctx)
+    tok += int(ctx.sum()); steps += 1
+    if el > %f: break
+print(json.dumps({"seconds": el, "steps": steps, "bytes": b, "tokens": tok}))
 """ % (ROOT, WORKLOAD, max_seconds)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
+        tail = r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "no output"
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + tail}
     rec = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": rec["bytes"] / rec["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"float64 numpy oracle, step 0 of {WORKLOAD}: first {rec['seqs']} of 64 sequences "
-                      f"({rec['tokens']} context tokens, all 32 q heads) in {rec['seconds']:.2f} s, 1 thread",
+            "sample": f"float64 numpy oracle on {WORKLOAD}: decode steps 0..{rec['steps'] - 1} in full "
+                      f"(64 sequences x 32 q heads each, {rec['tokens']} context tokens in total), "
+                      f"{rec['seconds']:.2f} s of decode time, 1 thread; appends untimed",
             "seconds": rec["seconds"]}
 
 
@@ -249,7 +259,7 @@ def run_ours(args, rank, world, local_rank):
 
     # the CPU oracle baseline runs first, in its own 1-thread process
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not (args.no_cpu_baseline or args.quick):
         cpu = cpu_baseline()
 
     torch.cuda.set_device(local_rank)
@@ -284,7 +294,7 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
     t_busy0 = time.time()
     i = 0
-    while time.time() - t_busy0 < 1.0:
+    while not args.quick and time.time() - t_busy0 < 1.0:
         step(i)
         i += 1
         if i % 64 == 0:
@@ -358,16 +368,18 @@ def run_ours(args, rank, world, local_rank):
                                partition_size=args.partition, workspace=ws, stream=stream)
         out_host.copy_(out, non_blocking=True)
         stream.synchronize()
-    for w in range(args.warmup):
-        e2e_step(w)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    te0 = time.perf_counter()
-    for k in range(args.steps):
-        e2e_step(args.warmup + k)
-    te1 = time.perf_counter()
-    e2e_s = te1 - te0
+    e2e_s = float("nan")
+    if not args.quick:
+        for w in range(args.warmup):
+            e2e_step(w)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        te0 = time.perf_counter()
+        for k in range(args.steps):
+            e2e_step(args.warmup + k)
+        te1 = time.perf_counter()
+        e2e_s = te1 - te0
     if world > 1:
         tt = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -400,6 +412,92 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# per-call figures of the other workloads
+# ---------------------------------------------------------------------------
+
+def run_other(args):
+    """Append / prefill / decode times of one workload, each call bracketed by
+    CUDA events on its stream, with L2 flushed (a 512 MB write) before every
+    step so that each call reads its inputs from HBM."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_decode_27_gb300 import binding as pa
+    from paged_kv_decode_27_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]()
+    kp, vp = wl.k_pool.to(dev), wl.v_pool.to(dev)
+    bt = wl.decode_block_tables.contiguous().to(dev)
+    pbt = wl.prefill_block_tables.contiguous().to(dev) if wl.prompt_lens else None
+    steps_in = [wl.step(t) for t in range(wl.steps)]
+    d_in = []
+    for st in steps_in:
+        d = {"slots": st.slot_mapping.to(dev), "kn": st.k_new.to(dev), "vn": st.v_new.to(dev),
+             "q": st.q.to(dev), "ctx": st.context_lens.to(dev)}
+        if wl.prompt_lens:
+            d.update(qp=st.q_prefill.to(dev), cu=st.cu_q_lens.to(dev), pctx=st.prefill_context_lens.to(dev),
+                     pout=torch.empty_like(st.q_prefill, device=dev))
+        d_in.append(d)
+    max_ctx = wl.max_context_len(wl.steps - 1)
+    S, hq, dh = wl.num_decode_seqs, wl.num_q_heads, wl.head_dim
+    ws = torch.empty(max(1, pa.pa_decode_workspace_size(S, hq, max_ctx, kp, args.partition)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((S, hq, dh), dtype=wl.dtype, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    rec = {"append": [], "prefill": [], "decode": []}
+
+    def step(t, timed):
+        d = d_in[t % wl.steps]
+        if timed:
+            flush.fill_(t & 0xFF)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        evs[0].record(stream)
+        pa.pa_append_kv(kp, vp, d["slots"], d["kn"], d["vn"], stream=stream)
+        evs[1].record(stream)
+        if wl.prompt_lens:
+            pa.pa_prefill_attention(d["pout"], d["qp"], kp, vp, pbt, d["cu"], d["pctx"], wl.scale,
+                                    max_q_len=max(wl.prompt_lens), max_context_len=max(wl.prompt_lens),
+                                    stream=stream)
+        evs[2].record(stream)
+        pa.pa_decode_attention(out, d["q"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
+                               partition_size=args.partition, workspace=ws, stream=stream)
+        evs[3].record(stream)
+        return evs
+    for w in range(args.warmup):
+        step(w, False)
+    torch.cuda.synchronize()
+    evl = [step(args.warmup + k, True) for k in range(args.steps)]
+    torch.cuda.synchronize()
+    for k, e in enumerate(evl):
+        rec["append"].append(e[0].elapsed_time(e[1]) * 1e3)
+        rec["prefill"].append(e[1].elapsed_time(e[2]) * 1e3)
+        rec["decode"].append(e[2].elapsed_time(e[3]) * 1e3)
+    med = {k: statistics.median(v) for k, v in rec.items()}
+    t_mid = (args.warmup + args.steps // 2) % wl.steps
+    dec_b = wl.decode_bytes(t_mid)
+    peak, kind = peak_hbm()
+    line = {"workload": wl.name, "description": wl.description, "steps": args.steps, "warmup": args.warmup,
+            "l2": "flushed before every step (512 MB write)",
+            "partition_tokens": pa.pa_decode_partition_size(S, max_ctx, kp, args.partition),
+            "append_us": med["append"], "append_gbs": wl.append_bytes() / (med["append"] * 1e-6) / 1e9,
+            "decode_us": med["decode"], "decode_p90_us": sorted(rec["decode"])[int(0.9 * (args.steps - 1))],
+            "decode_gbs": dec_b / (med["decode"] * 1e-6) / 1e9,
+            "decode_frac_of_hbm_peak": dec_b / (med["decode"] * 1e-6) / 1e9 / peak, "hbm_peak": peak,
+            "hbm_peak_kind": kind, "decode_bytes": dec_b,
+            "decode_tokens_per_s": S / ((med["append"] + med["decode"] + med["prefill"]) * 1e-6)}
+    if wl.prompt_lens:
+        fl = wl.prefill_flops()
+        line.update(prefill_us=med["prefill"], prefill_tflops=fl / (med["prefill"] * 1e-6) / 1e12,
+                    prefill_flops=fl)
+    line["device_status"] = pa.pa_device_status()
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -407,6 +505,11 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload != WORKLOAD:
+        if world > 1:
+            raise SystemExit("--workload other than the headline runs on one GPU")
+        run_other(args)
         return
     if world > 1:
         import torch
