@@ -189,6 +189,39 @@ PA_API int pa_prefill_attention(void* out, const void* q, const void* k_pool, co
                          int num_q_heads, int max_blocks_per_seq, int max_q_len,
                          int max_context_len, const pa_pool_desc* pool, void* stream);
 
+/* Bytes of the per-device array behind pa_decode_attention_noalloc. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * pa_decode_attention_noalloc -- pa_decode_attention for callers that cannot
+ * allocate device memory.  (The paper has no counterpart: this entry point
+ * exists for callers, not for the method.)
+ *
+ * Some callers cannot call cudaMalloc: a serving loop that may not allocate
+ * once it is running, an embedder that hands over only tensors it already
+ * owns, a plain C host without a device allocator.  This call takes the same
+ * arguments as pa_decode_attention minus the workspace and allocates nothing;
+ * the split-K partials go to a file-scope device array of
+ * PA_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library holds
+ * until the process exits.  The caller still passes every input and output.
+ *  - A shape whose partials need more than PA_NOALLOC_SCRATCH_BYTES
+ *    (see pa_decode_workspace_size) returns PA_ERR_INVALID with a message,
+ *    before anything is enqueued.  A larger partition_size needs less.
+ *  - The first call on a device that needs the array looks up its device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture.
+ *  - Every call on a device shares the array and it keeps the last call's
+ *    contents; nothing in it needs to start at zero.  Calls that overlap on
+ *    the GPU (e.g. on two streams) race on it: serialise them.
+ * Other errors as pa_decode_attention.
+ */
+PA_API int pa_decode_attention_noalloc(void* out, const void* q, const void* k_pool,
+                                       const void* v_pool, const int32_t* block_tables,
+                                       const int32_t* context_lens, float scale, int num_seqs,
+                                       int num_q_heads, int max_blocks_per_seq,
+                                       int max_context_len, int partition_size,
+                                       const pa_pool_desc* pool, void* stream);
+
 /*
  * pa_device_status -- read and clear the device status word of the current
  * device (bits PA_DEV_*).  Synchronises `stream` first.  Returns PA_OK when the

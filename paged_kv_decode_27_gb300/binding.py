@@ -213,3 +213,34 @@ def pa_device_status(stream=None) -> int:
     if rc not in (PA_OK, PA_ERR_DEVICE):
         raise PaError(rc, pa_last_error())
     return int(st.value)
+
+
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def pa_decode_attention_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                max_context_len: int, partition_size: int = 0, stream=None) -> None:
+    """pa_decode_attention for callers that cannot allocate device memory: no
+    workspace argument, and nothing is allocated here or in the library; the
+    split-K partials use the library's built-in 32 MiB per-device array.
+    Shapes needing more scratch raise PaError; calls overlapping on the GPU
+    share that array and must be serialised."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 3 and q.shape[2] == k_pool.shape[3], "q must be [S][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype == k_pool.dtype, "out/q shape or dtype mismatch")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
+    L = load_library()
+    fn = L.pa_decode_attention_noalloc
+    if fn.argtypes is None:
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.restype = i32
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, ctypes.POINTER(pa_pool_desc), vp]
+    _check(fn(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
+              float(scale), S, hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+              ctypes.byref(desc), _stream(stream)))

@@ -208,6 +208,13 @@ int check_decode_shape(int num_seqs, int num_q_heads, int max_blocks_per_seq, in
 
 }  // namespace
 
+namespace pa {
+int set_last_error(int code, const char* msg) {
+  t_err = msg;
+  return code;
+}
+}  // namespace pa
+
 extern "C" {
 
 int pa_version(void) { return PA_VERSION; }

@@ -49,6 +49,9 @@ struct PrefillArgs {
   int* status;
 };
 
+// Record `msg` as the calling thread's pa_last_error() and return `code`.
+int set_last_error(int code, const char* msg);
+
 cudaError_t launch_append(void* k_pool, void* v_pool, const int64_t* slot_mapping,
                           const void* k_new, const void* v_new, int num_tokens,
                           int num_kv_heads, int row_bytes, int num_blocks, int* status,
