@@ -134,8 +134,8 @@ PA_API int pa_decode_partition_size(int num_seqs, int max_context_len, int parti
  *
  * Work is split into partitions of `partition_size` tokens (split-K); a
  * sequence spanning several partitions has its partial softmax results merged
- * by log-sum-exp in a second kernel.  The result does not depend on the
- * partition beyond fp32 rounding.
+ * by log-sum-exp, by whichever of its partitions finishes last (one kernel).
+ * The result does not depend on the partition beyond fp32 rounding.
  *
  *   out               : [num_seqs][num_q_heads][D], written
  *   q                 : [num_seqs][num_q_heads][D]
@@ -149,13 +149,18 @@ PA_API int pa_decode_partition_size(int num_seqs, int max_context_len, int parti
  *                       of 16 in [16, 2048]
  *   workspace         : device scratch of >= pa_decode_workspace_size(...) bytes,
  *                       16-byte aligned (may be NULL when that size is 0).  Its
- *                       contents need no initialisation; two calls in flight at
- *                       once must not share it.
+ *                       first 256 KiB hold split-K completion counters that must
+ *                       be zero when a call starts: zero-fill the buffer once
+ *                       before its first use; every call that completes leaves
+ *                       them zero again, whatever shapes the calls have.  After
+ *                       a PA_DEV_WAIT_TIMEOUT report, zero-fill it again.  Two
+ *                       calls in flight at once must not share a workspace.
  * Errors: PA_ERR_INVALID for null or misaligned pointers, num_q_heads not a
  * multiple of num_kv_heads, max_context_len > max_blocks_per_seq*16, a bad
  * partition_size, a too-small workspace or a non-finite scale;
- * PA_ERR_UNSUPPORTED for head_dim not 64/128, G > 8, or a pool too large for
- * 32-bit row coordinates.
+ * PA_ERR_UNSUPPORTED for head_dim not 64/128, G > 8, a pool too large for
+ * 32-bit row coordinates, or split-K over more than 65536 (sequence, KV head)
+ * pairs in one call.
  */
 PA_API int pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
                         const int32_t* block_tables, const int32_t* context_lens,
@@ -211,8 +216,10 @@ PA_API int pa_prefill_attention(void* out, const void* q, const void* k_pool, co
  *    address (cudaGetSymbolAddress) with that device current; make that first
  *    call before any stream capture.
  *  - Every call on a device shares the array and it keeps the last call's
- *    contents; nothing in it needs to start at zero.  Calls that overlap on
- *    the GPU (e.g. on two streams) race on it: serialise them.
+ *    contents.  The split-K completion counters at its start must be zero
+ *    when a call begins: each call clears the ones it uses (an asynchronous
+ *    memset on `stream`) before its kernel.  Calls that overlap on the GPU
+ *    (e.g. on two streams) race on it: serialise them.
  * Other errors as pa_decode_attention.
  */
 PA_API int pa_decode_attention_noalloc(void* out, const void* q, const void* k_pool,

@@ -163,7 +163,8 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor
                         max_context_len: int, partition_size: int = 0,
                         workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """out, q: [S][H_q][D]; block_tables int32 [S][max_blocks]; context_lens int32 [S].
-    ``workspace`` (uint8 CUDA tensor) is allocated here when not given."""
+    ``workspace`` (uint8 CUDA tensor, zero-filled before its first use) is
+    allocated here, zero-filled, when not given."""
     desc = _pools(k_pool, v_pool)
     for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("context_lens", context_lens)):
         _cuda_contig(n, t)
@@ -176,7 +177,7 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor
     L = load_library()
     need = pa_decode_workspace_size(S, hq, max_context_len, k_pool, partition_size)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.pa_decode_attention(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                                  _ptr(context_lens), float(scale), S, hq, int(block_tables.shape[1]),

@@ -19,6 +19,7 @@ append_kv_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                  const int64_t* __restrict__ slot_mapping, const uint4* __restrict__ k_new,
                  const uint4* __restrict__ v_new, int num_tokens, int num_kv_heads,
                  int chunks_per_row, int num_blocks, int* status) {
+  allow_dependents();   // the decode/prefill that follows waits for our writes itself
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long per_tensor = static_cast<long long>(num_tokens) * num_kv_heads * chunks_per_row;
   if (idx >= per_tensor) return;

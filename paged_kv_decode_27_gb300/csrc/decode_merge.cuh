@@ -1,5 +1,7 @@
 // decode_merge.cuh -- merge the per-warp online-softmax states of one CTA and
-// store either the final output (single partition) or one split-K partial.
+// store either the final output (single partition) or one split-K partial;
+// for split-K, the CTA that finishes last for its (sequence, KV head) then
+// merges all partials (the log-sum-exp combine, fused into the decode kernel).
 //
 // Each warp leaves, for every query head h of the group (h < G <= 8):
 //   red_m[w][h]  running max of the log2-domain scores,
@@ -17,6 +19,7 @@ template <typename T, int W, int D>
 __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float* red_o,
                                                 const float* red_m, const float* red_l, int G,
                                                 int s, int kvh, int split, int n_splits) {
+  __shared__ int s_last;
   for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
     const int h = idx / D;
     const int d = idx - h * D;
@@ -44,6 +47,44 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
       if (d == 0) a.ws_lse[row] = (L > 0.f) ? M + log2f(L) : -INFINITY;
     }
   }
+  if (n_splits == 1) return;
+
+  // ---- split-K: the last CTA of this (sequence, KV head) merges every
+  // partition by log-sum-exp.  With M = max_p lse_p and w_p = 2^(lse_p - M),
+  // out = sum_p w_p o_p / sum_p w_p -- the softmax over the whole context.
+  __threadfence();                 // publish this CTA's partials device-wide
+  __syncthreads();
+  int* counter = a.ws_count + static_cast<size_t>(s) * a.num_kv_heads + kvh;
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(counter, 1);
+    __threadfence();
+    s_last = (prev == n_splits - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();                 // see the other partitions' partials
+  T* out = static_cast<T*>(a.out);
+  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    const int hq = kvh * G + h;
+    const size_t row0 = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.max_splits;
+    float M = -INFINITY;
+    for (int p = 0; p < n_splits; ++p) M = fmaxf(M, __ldcg(a.ws_lse + row0 + p));
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int p = 0; p < n_splits; ++p) {
+        const float lp = __ldcg(a.ws_lse + row0 + p);
+        if (lp == -INFINITY) continue;
+        const float w = exp2f(lp - M);
+        L += w;
+        O = fmaf(w, __ldcg(a.ws_o + (row0 + p) * D + d), O);
+      }
+    }
+    out[(static_cast<size_t>(s) * a.num_q_heads + hq) * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
+  }
+  // leave the counter at zero for the next call on this workspace
+  if (threadIdx.x == 0) *counter = 0;
 }
 
 // A sequence with an empty context produces zero rows for its heads.

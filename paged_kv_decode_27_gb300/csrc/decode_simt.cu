@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(W * 32) decode_simt_kernel(const DecodeArgs a)
   const int lane = threadIdx.x & 31;
   const int G = a.num_q_heads / a.num_kv_heads;
 
+  grid_dependency_wait();   // inputs may come from the kernel just before us
   const int ctx = checked_context(a, s, threadIdx.x == 0 && split == 0 && kvh == 0);
   const int nblk_seq = (ctx + kBlock - 1) / kBlock;
   const int n_splits = (nblk_seq + a.part_blocks - 1) / a.part_blocks;
@@ -137,8 +138,7 @@ template <typename T, int D>
 cudaError_t launch_simt_t(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int W = 4;
   dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-  decode_simt_kernel<T, D, W><<<grid, W * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(decode_simt_kernel<T, D, W>, grid, dim3(W * 32), 0, stream, a);
 }
 }  // namespace
 

@@ -21,8 +21,9 @@
 //    B-operand layout with movmatrix, and O^T += V^T P^T with V read through
 //    ldmatrix.trans.  Accumulators stay in registers.
 //  * The W warp states are merged in shared memory; the CTA writes the final
-//    row (one partition) or a normalised partial plus its log2-sum-exp2 for
-//    the log-sum-exp combine kernel.
+//    row (one partition) or a normalised partial plus its log2-sum-exp2; the
+//    last partition of a (sequence, KV head) to finish merges them all by
+//    log-sum-exp (see decode_merge.cuh).
 //
 // The last block of a sequence is partial: scores of positions past the
 // context are set to -inf and the matching V elements are zeroed, so stale
@@ -55,6 +56,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const int lane = threadIdx.x & 31;
   const int G = a.num_q_heads / a.num_kv_heads;
 
+  grid_dependency_wait();   // inputs may come from the kernel just before us
   const int ctx = checked_context(a, s, threadIdx.x == 0 && split == 0 && kvh == 0);
   const int nblk_seq = (ctx + kBlock - 1) / kBlock;
   const int n_splits = (nblk_seq + a.part_blocks - 1) / a.part_blocks;
@@ -293,8 +295,7 @@ cudaError_t launch_tc_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUte
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-  kern<<<grid, W * 32, smem, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(W * 32), smem, stream, kmap, vmap, a);
 }
 
 }  // namespace

@@ -27,6 +27,10 @@ constexpr int kGb300Sms = 152;
 // (sequence, KV head, partition) units, i.e. several CTAs per SM.
 constexpr long long kTargetUnits = 4LL * kGb300Sms;
 constexpr int kMaxPartition = 2048;   // 32 blocks per warp of a 4-warp CTA
+// Split-K completion counters occupy a fixed region at the start of the
+// workspace, so no shape's partials ever overlap another shape's counters.
+constexpr int kMaxCounters = 65536;   // (sequence, KV head) pairs per split-K call
+constexpr size_t kCounterBytes = kMaxCounters * sizeof(int);
 
 thread_local std::string t_err;
 
@@ -102,16 +106,17 @@ int max_splits_for(int max_context_len, int part_blocks) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// [counters: kCounterBytes][partial outputs: rows x D fp32][partial lse: rows fp32]
 struct WsLayout {
-  size_t o_bytes, lse_off, total;
+  size_t o_off, lse_off, total;
 };
 
 WsLayout ws_layout(int num_seqs, int num_q_heads, int max_splits, int head_dim) {
   WsLayout w{0, 0, 0};
   if (max_splits <= 1) return w;
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_splits;
-  w.o_bytes = rows * head_dim * sizeof(float);
-  w.lse_off = align256(w.o_bytes);
+  w.o_off = kCounterBytes;
+  w.lse_off = align256(w.o_off + rows * head_dim * sizeof(float));
   w.total = w.lse_off + rows * sizeof(float);
   return w;
 }
@@ -282,6 +287,9 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
   const int part_blocks = part / PA_BLOCK_SIZE;
   const int max_splits = max_splits_for(max_context_len, part_blocks);
   const WsLayout ws = ws_layout(num_seqs, num_q_heads, max_splits, pool->head_dim);
+  if (ws.total > 0 && static_cast<long long>(num_seqs) * pool->num_kv_heads > kMaxCounters)
+    return fail(PA_ERR_UNSUPPORTED, "split-K over more than %d (sequence, KV head) pairs in one call",
+                kMaxCounters);
   if (ws.total > 0) {
     if (!workspace) return fail(PA_ERR_INVALID, "workspace of %zu bytes required, got NULL", ws.total);
     if (workspace_bytes < ws.total)
@@ -308,7 +316,8 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
   a.num_blocks = pool->num_blocks;
   a.part_blocks = part_blocks;
   a.max_splits = max_splits;
-  a.ws_o = ws.total ? static_cast<float*>(workspace) : nullptr;
+  a.ws_count = ws.total ? static_cast<int*>(workspace) : nullptr;
+  a.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_off) : nullptr;
   a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
   a.status = status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -323,10 +332,6 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
     e = pa::launch_decode_tc(a, pool->dtype, kmap, vmap, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (max_splits > 1) {
-    e = pa::launch_combine(a, pool->dtype, st);
-    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  }
   return PA_OK;
 }
 

@@ -29,6 +29,7 @@ struct DecodeArgs {
   int max_splits;          // ceil(ceil(max_context_len / 16) / part_blocks)
   float* ws_o;             // [S][H_q][max_splits][D]  normalised partial outputs
   float* ws_lse;           // [S][H_q][max_splits]     partial log2-sum-exp2
+  int* ws_count;           // [S][H_kv] partitions finished (zero between calls)
   int* status;             // device status word (PA_DEV_* bits)
 };
 
@@ -63,9 +64,6 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int dtype, const CUtensorMap& 
 
 // CUDA-core decode (any supported dtype; the fp32 path).
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t stream);
-
-// Log-sum-exp merge of the split-K partials into out.
-cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t stream);
 
 // Tensor-core causal prefill (bf16/fp16 pools, D in {64, 128}).
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,

@@ -14,8 +14,9 @@
 //
 // The array is PA_NOALLOC_SCRATCH_BYTES (32 MiB) per device.  It is part of
 // the library's module, so every GPU that loads the library holds it until the
-// process exits.  Nothing in it has to start at zero: each partial the combine
-// kernel reads is written earlier by the same call.
+// process exits.  Only the split-K completion counters at its start must be
+// zero when a call begins; each call clears the ones it uses.  The partials
+// the merge reads are written earlier by the same call.
 #include <cstdio>
 #include <mutex>
 
@@ -83,6 +84,19 @@ extern "C" PA_API int pa_decode_attention_noalloc(void* out, const void* q, cons
       return pa::set_last_error(PA_ERR_CUDA, msg);
     }
     ws_bytes = PA_NOALLOC_SCRATCH_BYTES;
+    // The split-K completion counters at the start of the array must be zero
+    // when the kernel starts; clear the ones this call uses (no allocation).
+    // (batches beyond the 65536-entry counter region are refused by
+    // pa_decode_attention below, so nothing is enqueued for them)
+    const long long pairs = static_cast<long long>(num_seqs) * pool->num_kv_heads;
+    if (pairs <= 65536)
+      e = cudaMemsetAsync(ws, 0, static_cast<size_t>(pairs) * sizeof(int), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+      char msg[200];
+      snprintf(msg, sizeof(msg), "pa_decode_attention_noalloc: clearing the counters failed: %s",
+               cudaGetErrorString(e));
+      return pa::set_last_error(PA_ERR_CUDA, msg);
+    }
   }
   // Every other check, and the launches, are those of pa_decode_attention.
   return pa_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, scale, num_seqs,

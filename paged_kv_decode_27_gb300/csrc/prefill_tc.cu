@@ -53,6 +53,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const int G = a.num_q_heads / a.num_kv_heads;
   const int kvh = hq / G;
 
+  grid_dependency_wait();   // the prompt's K/V were appended by the kernel before us
   const int q0 = __ldg(a.cu_q_lens + s);
   const int n = __ldg(a.cu_q_lens + s + 1) - q0;
   int c = __ldg(a.context_lens + s);
@@ -293,8 +294,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap& kmap, cons
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.max_q_len + 63) / 64, a.num_q_heads, a.num_seqs);
-  kern<<<grid, 128, smem, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(128), smem, stream, kmap, vmap, a);
 }
 }  // namespace
 

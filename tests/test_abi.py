@@ -111,8 +111,8 @@ def test_workspace_size_and_partition(lib):
     assert lib.pa_decode_partition_size(64, 8224, 0, ctypes.byref(d)) == 512
     n = lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(d))
     rows = 64 * 32 * 17
-    o = rows * 128 * 4
-    assert n == ((o + 255) // 256) * 256 + rows * 4
+    o_end = 256 * 1024 + rows * 128 * 4          # counters, then partial outputs
+    assert n == ((o_end + 255) // 256) * 256 + rows * 4
     # few units: the partition shrinks (8 sequences of <= 2063 tokens -> 128)
     assert lib.pa_decode_partition_size(8, 2063, 0, ctypes.byref(_desc(d=64))) == 128
     # one partition covers everything: no workspace
