@@ -52,34 +52,37 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
   // ---- split-K: the last CTA of this (sequence, KV head) merges every
   // partition by log-sum-exp.  With M = max_p lse_p and w_p = 2^(lse_p - M),
   // out = sum_p w_p o_p / sum_p w_p -- the softmax over the whole context.
-  __threadfence();                 // publish this CTA's partials device-wide
+  // Release/acquire: the CTA barrier orders every thread's partial stores
+  // before thread 0's acq_rel atomic; the last CTA's atomic acquires the other
+  // partitions' stores, and the second barrier passes that on to its threads.
   __syncthreads();
   int* counter = a.ws_count + static_cast<size_t>(s) * a.num_kv_heads + kvh;
   if (threadIdx.x == 0) {
-    const int prev = atomicAdd(counter, 1);
-    __threadfence();
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
     s_last = (prev == n_splits - 1);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();                 // see the other partitions' partials
   T* out = static_cast<T*>(a.out);
   for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
     const int h = idx / D;
     const int d = idx - h * D;
     const int hq = kvh * G + h;
     const size_t row0 = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.max_splits;
-    float M = -INFINITY;
-    for (int p = 0; p < n_splits; ++p) M = fmaxf(M, __ldcg(a.ws_lse + row0 + p));
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int p = 0; p < n_splits; ++p) {
-        const float lp = __ldcg(a.ws_lse + row0 + p);
-        if (lp == -INFINITY) continue;
-        const float w = exp2f(lp - M);
-        L += w;
-        O = fmaf(w, __ldcg(a.ws_o + (row0 + p) * D + d), O);
-      }
+    // one pass with a running max: loads of different partitions are independent
+    float M = -INFINITY, L = 0.f, O = 0.f;
+#pragma unroll 4
+    for (int p = 0; p < n_splits; ++p) {
+      const float lp = __ldcg(a.ws_lse + row0 + p);
+      const float op = __ldcg(a.ws_o + (row0 + p) * D + d);
+      if (lp == -INFINITY) continue;
+      const float mn = fmaxf(M, lp);
+      const float r = exp2f(M - mn);      // 0 while M is still -inf
+      const float w = exp2f(lp - mn);
+      L = fmaf(L, r, w);
+      O = fmaf(O, r, w * op);
+      M = mn;
     }
     out[(static_cast<size_t>(s) * a.num_q_heads + hq) * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
   }

@@ -287,7 +287,7 @@ template <typename T, int D>
 cudaError_t launch_tc_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         cudaStream_t stream) {
   constexpr int W = 4;
-  constexpr int NS = (D == 128) ? 3 : 4;
+  constexpr int NS = (D == 128) ? 2 : 4;   // 3 CTAs per SM either way (64 KB of stages)
   constexpr int STAGE = 2 * (D / 64) * 16 * 128;
   static_assert(W * 8 * D * 4 + W * 16 * 4 <= W * NS * STAGE, "merge buffer must fit");
   const int smem = W * NS * STAGE + 1024;

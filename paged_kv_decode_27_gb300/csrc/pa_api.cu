@@ -89,7 +89,7 @@ int* status_ptr() {
 
 int choose_partition(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
   if (requested > 0) return requested;
-  int p = 512;
+  int p = 1024;
   while (p > 64) {
     const long long units =
         static_cast<long long>(num_seqs) * num_kv_heads * ((max_context_len + p - 1) / p);

@@ -107,10 +107,10 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
 
 def test_workspace_size_and_partition(lib):
     d = _desc(d=128)
-    # batch 64, 8 KV heads, contexts to 8224: 512-token partitions, 17 splits
-    assert lib.pa_decode_partition_size(64, 8224, 0, ctypes.byref(d)) == 512
+    # batch 64, 8 KV heads, contexts to 8224: 1024-token partitions, 9 splits
+    assert lib.pa_decode_partition_size(64, 8224, 0, ctypes.byref(d)) == 1024
     n = lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(d))
-    rows = 64 * 32 * 17
+    rows = 64 * 32 * 9
     o_end = 256 * 1024 + rows * 128 * 4          # counters, then partial outputs
     assert n == ((o_end + 255) // 256) * 256 + rows * 4
     # few units: the partition shrinks (8 sequences of <= 2063 tokens -> 128)
