@@ -376,7 +376,7 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   CUtensorMap kmap, vmap;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
-  cudaError_t e = pa::launch_prefill_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pa::launch_prefill_umma(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PA_OK;
 }

@@ -65,8 +65,9 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int dtype, const CUtensorMap& 
 // CUDA-core decode (any supported dtype; the fp32 path).
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t stream);
 
-// Tensor-core causal prefill (bf16/fp16 pools, D in {64, 128}).
-cudaError_t launch_prefill_tc(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, cudaStream_t stream);
+// Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).
+cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, cudaStream_t stream);
+
 
 }  // namespace pa
