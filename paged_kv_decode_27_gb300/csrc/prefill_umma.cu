@@ -24,9 +24,10 @@
 //      warps 9/10 MMA issuers for tile A / B: S = Q K^T (M=128, N=128, K=D; Q
 //                 and K from shared memory) and O += P V (M=128, N=D, K=128; P
 //                 from tensor memory, V read MN-major straight from its pool
-//                 layout), each as soon as its inputs are ready.  One issuer
-//                 per tile, because issuing stalls while the tensor pipe is
-//                 busy and must not hold up the other tile.
+//                 layout).  One issuer per tile, because issuing stalls while
+//                 the tensor pipe is busy and must not hold up the other tile.
+//    Producer and issuers block in mbarrier.try_wait on the next input they
+//    need, leaving the issue slots to the softmax warps.
 //    N = 128 keys per S tile: with the A operand in shared memory a narrower
 //    MMA costs as much as this one.
 //  * Tensor memory (all 512 columns): per tile one S/P buffer of 128 columns
@@ -226,47 +227,35 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       if (h < NBOX) tma_load_2d(dst + h * L::HALF_KT + b * 2048, map, h * 64, y, bar, policy);
       __syncwarp();
     };
+    // Fixed order K_0 V_0 K_1 V_1 ...: K_{j+2} reuses the stage freed by the S
+    // MMAs of tile j, V_{j+2} the one freed by its PV MMAs.  The warp blocks
+    // (suspended in mbarrier.try_wait) on exactly the next release it needs.
+    auto stage_free = [&](bool is_k, int j) -> bool {   // all lanes
+      if (j < kStages) return true;
+      const int jp = j - kStages;
+      bool ok2 = true;
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (jp < nkt_g[g])
+          ok2 = ok2 && !abort_sh &&
+                mbar_wait_bounded(is_k ? k_empty(g, jp % kStages) : v_empty(g, jp % kStages), (jp / kStages) & 1);
+      return __all_sync(0xffffffffu, ok2) != 0;
+    };
     int next_k = 0, next_v = 0;
     load_chunk(0);
-    uint64_t t_last = global_timer_ns();
-    for (uint32_t spin = 0; next_v < n_kt; ++spin) {
-      bool progressed = false;
-      // a stage is free once every tile that read its previous contents is done with it
-      auto stage_free = [&](bool is_k, int j) {
-        if (j < kStages) return true;
-        const int jp = j - kStages;
-        bool ok2 = true;
-#pragma unroll
-        for (int g = 0; g < 2; ++g)
-          if (jp < nkt_g[g])
-            ok2 = ok2 && mbar_test_wait(is_k ? k_empty(g, jp % kStages) : v_empty(g, jp % kStages),
-                                        (jp / kStages) & 1);
-        return ok2;
-      };
-      const bool k_ready = next_k < n_kt && stage_free(true, next_k);
-      if (__all_sync(0xffffffffu, k_ready)) {
-        load_tile(&kmap, sK + (next_k % kStages) * L::KT_BYTES, k_full(next_k % kStages), next_k);
-        ++next_k;
-        progressed = true;
+    for (int j = 0; j < n_kt; ++j) {
+      if (!stage_free(true, j)) {
+        abort_sh = 1;
+        break;
       }
-      const bool v_ready = next_v < next_k && stage_free(false, next_v);
-      if (__all_sync(0xffffffffu, v_ready)) {
-        load_tile(&vmap, sV + (next_v % kStages) * L::KT_BYTES, v_full(next_v % kStages), next_v);
-        ++next_v;
-        progressed = true;
+      load_tile(&kmap, sK + (j % kStages) * L::KT_BYTES, k_full(j % kStages), j);
+      next_k = j + 1;
+      if (!stage_free(false, j)) {
+        abort_sh = 1;
+        break;
       }
-      if (progressed) {
-        t_last = global_timer_ns();
-      } else {
-        __nanosleep(32);
-        if ((spin & 15u) == 0) {
-          const bool give_up = abort_sh || global_timer_ns() - t_last > 1000000000ull;
-          if (__any_sync(0xffffffffu, give_up)) {
-            abort_sh = 1;
-            break;
-          }
-        }
-      }
+      load_tile(&vmap, sV + (j % kStages) * L::KT_BYTES, v_full(j % kStages), j);
+      next_v = j + 1;
     }
     if (abort_sh && lane == 0) {
       // let the copies still in flight land before the CTA can exit
@@ -281,84 +270,64 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     const uint32_t tt = tmem + g * L::TMEM_TILE;
     const uint32_t id_s = umma_idesc_f16(kRows, kKeys, kBf16, false, false);
     const uint32_t id_o = umma_idesc_f16(kRows, D, kBf16, false, true);
+    // With one S/P buffer per tile the order is fixed -- S_0, PV_0, S_1, PV_1,
+    // ... -- so the warp blocks (suspended in mbarrier.try_wait, taking no
+    // issue slots from the softmax warps) on exactly the next input it needs.
     bool ok = true;
-    int next_s = 0, next_pv = 0;
     const int my_nkt = nkt_g[g];
-    uint64_t t_last = global_timer_ns();
-    for (uint32_t spin = 0; next_pv < my_nkt; ++spin) {
-      bool progressed = false;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
+    };
+    for (int j = 0; j < my_nkt && ok; ++j) {
+      const int st = j % kStages;
       // S_j = Q K_j^T once K_j has landed and PV_{j-1} (which read P from the
       // same columns) has completed
-      if (next_s < my_nkt) {
-        const int j = next_s;
-        const int st = j % kStages;
-        const bool ready = mbar_test_wait(k_full(st), (j / kStages) & 1) &&
-                           (j < 1 || mbar_test_wait(pv_done(g), (j - 1) & 1));
-        if (__all_sync(0xffffffffu, ready)) {
-          tc_fence_after_sync();
-          if (lane == 0) {
-            const uint32_t qbase = sQ + g * L::Q_BYTES;
-            const uint32_t kbase = sK + st * L::KT_BYTES;
+      ok = wait_all(k_full(st), (j / kStages) & 1) && (j < 1 || wait_all(pv_done(g), (j - 1) & 1));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (lane == 0) {
+        const uint32_t qbase = sQ + g * L::Q_BYTES;
+        const uint32_t kbase = sK + st * L::KT_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t da = umma_desc_sw128(qbase + (kk >> 2) * L::HALF_Q + (kk & 3) * 32, 16, 1024);
-              const uint64_t db = umma_desc_sw128(kbase + (kk >> 2) * L::HALF_KT + (kk & 3) * 32, 16, 1024);
-              umma_f16(tt + L::TMEM_S, da, db, id_s, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(s_full(g));
-            umma_commit(k_empty(g, st));
-          }
-          __syncwarp();
-          ++next_s;
-          progressed = true;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t da = umma_desc_sw128(qbase + (kk >> 2) * L::HALF_Q + (kk & 3) * 32, 16, 1024);
+          const uint64_t db = umma_desc_sw128(kbase + (kk >> 2) * L::HALF_KT + (kk & 3) * 32, 16, 1024);
+          umma_f16(tt + L::TMEM_S, da, db, id_s, kk > 0 ? 1u : 0u);
         }
+        umma_commit(s_full(g));
+        umma_commit(k_empty(g, st));
       }
-      // O += P_j V_j once the softmax has written P and V_j has landed
-      if (next_pv < next_s) {
-        const int j = next_pv;
-        const int st = j % kStages;
-        const bool ready = mbar_test_wait(p_full(g), j & 1) && mbar_test_wait(v_full(st), (j / kStages) & 1);
-        if (__all_sync(0xffffffffu, ready)) {
-          const uint32_t vbase = sV + st * L::KT_BYTES;
-          const int pb = c >> 4;
-          if ((c & 15) && pb / kBlocksPerTile == j) {
-            // value rows past the context read as zero (both issuers write the
-            // same zeros; each does it before its own PV reads the tile)
-            const int r0 = c & 15;
-            for (int idx = lane; idx < (16 - r0) * NBOX * 8; idx += 32) {
-              const int row = (pb % kBlocksPerTile) * 16 + r0 + idx / (NBOX * 8);
-              const int rem = idx % (NBOX * 8);
-              const uint32_t addr = vbase + (rem >> 3) * L::HALF_KT + row * 128 + ((rem & 7) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
-            }
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-          tc_fence_after_sync();
-          if (lane == 0) {
-            const uint32_t ptm = tt + L::TMEM_S;   // P: kKeys/2 columns of packed pairs
+      __syncwarp();
+      // O += P_j V_j once V_j has landed and the softmax has written P_j
+      ok = wait_all(v_full(st), (j / kStages) & 1) && wait_all(p_full(g), j & 1);
+      if (!ok) break;
+      const uint32_t vbase = sV + st * L::KT_BYTES;
+      const int pb = c >> 4;
+      if ((c & 15) && pb / kBlocksPerTile == j) {
+        // value rows past the context read as zero (both issuers write the
+        // same zeros; each does it before its own PV reads the tile)
+        const int r0 = c & 15;
+        for (int idx = lane; idx < (16 - r0) * NBOX * 8; idx += 32) {
+          const int row = (pb % kBlocksPerTile) * 16 + r0 + idx / (NBOX * 8);
+          const int rem = idx % (NBOX * 8);
+          const uint32_t addr = vbase + (rem >> 3) * L::HALF_KT + row * 128 + ((rem & 7) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      tc_fence_after_sync();
+      if (lane == 0) {
+        const uint32_t ptm = tt + L::TMEM_S;   // P: kKeys/2 columns of packed pairs
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t db = umma_desc_sw128(vbase + kk * 2048, L::HALF_KT, 1024);
-              umma_f16_tmem_a(tt + L::TMEM_O, ptm + kk * 8, db, id_o, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(pv_done(g));
-            umma_commit(v_empty(g, st));
-          }
-          __syncwarp();
-          ++next_pv;
-          progressed = true;
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t db = umma_desc_sw128(vbase + kk * 2048, L::HALF_KT, 1024);
+          umma_f16_tmem_a(tt + L::TMEM_O, ptm + kk * 8, db, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
+        umma_commit(pv_done(g));
+        umma_commit(v_empty(g, st));
       }
-      if (progressed) {
-        t_last = global_timer_ns();
-      } else if ((spin & 15u) == 0) {
-        const bool give_up = abort_sh || global_timer_ns() - t_last > 1000000000ull;
-        if (__any_sync(0xffffffffu, give_up)) {
-          ok = false;
-          break;
-        }
-      }
+      __syncwarp();
     }
     if (!ok) abort_sh = 1;
     // every MMA issued by this warp has completed before the CTA tears down
@@ -430,13 +399,14 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           break;
         }
         tc_fence_after_sync();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: the row of S is still live
+          float o[16];
+          tmem_ld16(tO + cc * 16, o);
+          uint32_t ob[16];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= factor;
-          tmem_st32(tO + cc * 32, o);
+          for (int i = 0; i < 16; ++i) ob[i] = __float_as_uint(o[i] * factor);
+          tmem_st16_u(tO + cc * 16, ob);
         }
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
