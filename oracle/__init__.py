@@ -2,7 +2,8 @@
 
 Test infrastructure: only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may use it.  The CUDA path never imports it.
-Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle.py``.
+Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle.py``
+and ``tests/test_oracle_int8.py``.
 """
 from .paged_attention import (  # noqa: F401
     BLOCK_SIZE,
@@ -14,4 +15,11 @@ from .paged_attention import (  # noqa: F401
     gather_contiguous,
     kv_cache_bytes,
     prefill_ref,
+)
+from .kv_int8 import (  # noqa: F401,E402
+    append_int8_ref,
+    decode_int8_ref,
+    dequantize_rows_int8,
+    gather_dequantized,
+    quantize_rows_int8,
 )

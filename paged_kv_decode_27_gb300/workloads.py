@@ -73,6 +73,10 @@ class Workload:
     factor: float = 1.0
     description: str = ""
     extra: dict = field(default_factory=dict)
+    # INT8 cache only: k_pool / v_pool then hold int8 codes and these the
+    # float32 scale of every (block, head, slot) row
+    k_scales: Optional[torch.Tensor] = None   # float32 [N_blk][H_kv][16]
+    v_scales: Optional[torch.Tensor] = None
 
     # ---- derived geometry -------------------------------------------------
     @property
@@ -85,7 +89,20 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
+        """Bytes of one q / out / new K/V element (the activation dtype)."""
         return torch.tensor([], dtype=self.dtype).element_size()
+
+    @property
+    def kv_int8(self) -> bool:
+        return self.k_pool.dtype == torch.int8
+
+    @property
+    def kv_row_bytes(self) -> int:
+        """Pool bytes of one (token, KV head) row: D elements, plus the float32
+        scale of an INT8 cache."""
+        if self.kv_int8:
+            return self.head_dim + 4
+        return self.head_dim * self.elem_bytes
 
     @property
     def decode_block_tables(self) -> torch.Tensor:
@@ -160,7 +177,7 @@ class Workload:
         tokens, q and out, the block ids read and the context lengths."""
         ctx = self.context_lens(t).to(torch.int64)
         e = self.elem_bytes
-        kv = int(ctx.sum()) * 2 * self.num_kv_heads * self.head_dim * e
+        kv = int(ctx.sum()) * 2 * self.num_kv_heads * self.kv_row_bytes
         qo = 2 * self.num_decode_seqs * self.num_q_heads * self.head_dim * e
         ids = 4 * int(((ctx + BLOCK_SIZE - 1) // BLOCK_SIZE).sum()) + 4 * self.num_decode_seqs
         return kv + qo + ids
@@ -168,8 +185,9 @@ class Workload:
     def append_bytes(self, t: int = 0) -> int:
         """Read new K/V + slots, write the same K/V into the pool."""
         st_tokens = self.num_decode_seqs + (sum(self.prompt_lens) if self.prompt_lens else 0)
-        row = self.num_kv_heads * self.head_dim * self.elem_bytes
-        return 2 * (2 * st_tokens * row) + 8 * st_tokens
+        row_in = self.num_kv_heads * self.head_dim * self.elem_bytes
+        row_out = self.num_kv_heads * self.kv_row_bytes
+        return 2 * st_tokens * (row_in + row_out) + 8 * st_tokens
 
     def prefill_flops(self) -> int:
         """4*D flops per (query, key, q-head) pair under the causal mask."""
@@ -220,6 +238,24 @@ def _pool(n_blk, hkv, d, dtype, factor, g) -> torch.Tensor:
     return x.to(dtype).contiguous()
 
 
+def _pool_int8(n_blk, hkv, d, factor, g):
+    """An INT8 cache drawn directly: codes uniform in [-127, 127], one float32
+    scale per (block, head, slot) uniform in [2, 4] * factor / 127 (the range
+    of max|x| / 127 for D values of N(0, factor^2))."""
+    codes = torch.randint(-127, 128, (n_blk, hkv, BLOCK_SIZE, d), generator=g, dtype=torch.int16)
+    scales = (torch.rand((n_blk, hkv, BLOCK_SIZE), generator=g) * 2.0 + 2.0) * (factor / 127.0)
+    return codes.to(torch.int8).contiguous(), scales.to(torch.float32).contiguous()
+
+
+def _kv_pools(n_blk, hkv, d, dtype, factor, g, kv: str):
+    """(k_pool, v_pool, k_scales, v_scales) of a float or an INT8 cache."""
+    if kv == "int8":
+        kc, ks = _pool_int8(n_blk, hkv, d, factor, g)
+        vc, vs = _pool_int8(n_blk, hkv, d, factor, g)
+        return kc, vc, ks, vs
+    return _pool(n_blk, hkv, d, dtype, factor, g), _pool(n_blk, hkv, d, dtype, factor, g), None, None
+
+
 # --------------------------------------------------------------------------
 # The five workloads.  Names say what each is; ids only pick the seed.
 # --------------------------------------------------------------------------
@@ -243,40 +279,47 @@ def tiny_fp32() -> Workload:
 
 def _multi_step(cid: int, name: str, S: int, hq: int, hkv: int, d: int, steps: int,
                 ctx0: torch.Tensor, factor: float, dtype=torch.bfloat16,
-                description: str = "") -> Workload:
+                description: str = "", kv: str = "float") -> Workload:
     g = torch.Generator().manual_seed(1000 + cid)
     g_ctx_consumed = ctx0  # drawn by the caller from the same generator
     need = [_blocks_for(int(c) + steps - 1) for c in g_ctx_consumed]
     pool_blocks = int(math.ceil(1.25 * sum(need)))
     bt = _assign_blocks(need, pool_blocks, g)
-    k_pool = _pool(pool_blocks, hkv, d, dtype, factor, g)
-    v_pool = _pool(pool_blocks, hkv, d, dtype, factor, g)
+    k_pool, v_pool, k_scales, v_scales = _kv_pools(pool_blocks, hkv, d, dtype, factor, g, kv)
     return Workload(name=name, config_id=cid, dtype=dtype, num_q_heads=hq, num_kv_heads=hkv,
                     head_dim=d, scale=1.0 / math.sqrt(d), steps=steps, k_pool=k_pool,
                     v_pool=v_pool, block_tables=bt, ctx0=ctx0.to(torch.int32),
-                    decode_rows=slice(0, S), factor=factor, description=description)
+                    decode_rows=slice(0, S), factor=factor, description=description,
+                    k_scales=k_scales, v_scales=v_scales)
 
 
-def llama32_1b_decode(steps: int = 16) -> Workload:
+def llama32_1b_decode(steps: int = 16, kv: str = "float") -> Workload:
     """Llama-3.2-1B-shaped decode, bf16: batch 8, h_q=32, h_kv=8, D=64,
-    contexts uniform in [128, 2048], pool 1.25x the need, values N(0,1)*0.5."""
+    contexts uniform in [128, 2048], pool 1.25x the need, values N(0,1)*0.5.
+    ``kv="int8"``: the same batch over an INT8 cache."""
     cid = 2
     gc = torch.Generator().manual_seed(1000 + cid + 500)
     ctx0 = torch.randint(128, 2048 + 1, (8,), generator=gc)
-    return _multi_step(cid, "llama32_1b_decode", 8, 32, 8, 64, steps, ctx0, 0.5,
-                       description="Llama-3.2-1B-shaped decode, bf16, batch 8")
+    name = "llama32_1b_decode" + ("_int8" if kv == "int8" else "")
+    return _multi_step(cid, name, 8, 32, 8, 64, steps, ctx0, 0.5, kv=kv,
+                       description="Llama-3.2-1B-shaped decode, bf16, batch 8" +
+                       (", INT8 KV cache" if kv == "int8" else ""))
 
 
-def llama3_8b_decode(steps: int = 32, batch: int = 64) -> Workload:
+def llama3_8b_decode(steps: int = 32, batch: int = 64, kv: str = "float") -> Workload:
     """Llama-3-8B-shaped decode, bf16: batch 64, h_q=32, h_kv=8, D=128,
-    contexts log-uniform in [512, 8192], randomly permuted pool (1.25x)."""
+    contexts log-uniform in [512, 8192], randomly permuted pool (1.25x).
+    ``kv="int8"``: the same batch (contexts, tables, per-step q and new K/V)
+    over an INT8 cache."""
     cid = 3
     gc = torch.Generator().manual_seed(1000 + cid + 500)
     u = torch.rand((batch,), generator=gc, dtype=torch.float64)
     ctx0 = torch.floor(torch.exp(math.log(512) + u * (math.log(8192) - math.log(512))))
     ctx0 = ctx0.clamp(512, 8192).to(torch.int64)
-    return _multi_step(cid, "llama3_8b_decode", batch, 32, 8, 128, steps, ctx0, 1.0,
-                       description="Llama-3-8B-shaped decode, bf16, batch %d" % batch)
+    name = "llama3_8b_decode" + ("_int8" if kv == "int8" else "")
+    return _multi_step(cid, name, batch, 32, 8, 128, steps, ctx0, 1.0, kv=kv,
+                       description="Llama-3-8B-shaped decode, bf16, batch %d" % batch +
+                       (", INT8 KV cache" if kv == "int8" else ""))
 
 
 def prefix_shared_8k() -> Workload:
@@ -326,14 +369,17 @@ WORKLOADS = {
     "llama3_8b_decode": llama3_8b_decode,
     "prefix_shared_8k": prefix_shared_8k,
     "mixed_mistral7b": mixed_mistral7b,
+    "llama32_1b_decode_int8": lambda: llama32_1b_decode(kv="int8"),
+    "llama3_8b_decode_int8": lambda: llama3_8b_decode(kv="int8"),
 }
 
 
 def small_random(seed: int, num_seqs: int, max_ctx: int, hq: int, hkv: int, d: int,
                  dtype: torch.dtype = torch.bfloat16, extra_blocks: int = 3,
-                 ctx: Optional[List[int]] = None) -> Workload:
+                 ctx: Optional[List[int]] = None, kv: str = "float") -> Workload:
     """A small ad-hoc workload for edge-case tests (ragged contexts, small
-    pools).  One step; contexts uniform in [1, max_ctx] unless given."""
+    pools).  One step; contexts uniform in [1, max_ctx] unless given.
+    ``kv="int8"`` draws an INT8 cache (q and new K/V stay ``dtype``)."""
     g = torch.Generator().manual_seed(seed)
     if ctx is None:
         ctx_t = torch.randint(1, max_ctx + 1, (num_seqs,), generator=g)
@@ -342,9 +388,9 @@ def small_random(seed: int, num_seqs: int, max_ctx: int, hq: int, hkv: int, d: i
     need = [max(1, _blocks_for(int(c))) for c in ctx_t]
     pool_blocks = sum(need) + extra_blocks
     bt = _assign_blocks(need, pool_blocks, g)
-    k_pool = _pool(pool_blocks, hkv, d, dtype, 1.0, g)
-    v_pool = _pool(pool_blocks, hkv, d, dtype, 1.0, g)
+    k_pool, v_pool, k_scales, v_scales = _kv_pools(pool_blocks, hkv, d, dtype, 1.0, g, kv)
     return Workload(name="small_random_%d" % seed, config_id=10_000 + seed, dtype=dtype,
                     num_q_heads=hq, num_kv_heads=hkv, head_dim=d, scale=1.0 / math.sqrt(d),
                     steps=1, k_pool=k_pool, v_pool=v_pool, block_tables=bt,
-                    ctx0=ctx_t.to(torch.int32), decode_rows=slice(0, len(need)))
+                    ctx0=ctx_t.to(torch.int32), decode_rows=slice(0, len(need)),
+                    k_scales=k_scales, v_scales=v_scales)

@@ -96,3 +96,19 @@ def test_byte_accounting():
     wl = W.tiny_fp32()
     # KV: (17+40) tokens * 2 (K,V) * 2 heads * 64 * 4 B; q,out: 2*2*4*64*4; ids: 5 blocks + 2 lens
     assert wl.decode_bytes(0) == 57 * 2 * 2 * 64 * 4 + 2 * 2 * 4 * 64 * 4 + 4 * 5 + 4 * 2
+
+
+def test_int8_cache_draw():
+    wl = W.small_random(3, 4, 300, 8, 2, 64, kv="int8")
+    assert wl.kv_int8 and wl.k_pool.dtype == torch.int8 and wl.v_pool.dtype == torch.int8
+    assert wl.k_scales.shape == wl.k_pool.shape[:3] and wl.k_scales.dtype == torch.float32
+    assert int(wl.k_pool.min()) >= -127 and int(wl.k_pool.max()) <= 127
+    assert float(wl.k_scales.min()) >= 2.0 / 127 and float(wl.v_scales.max()) <= 4.0 / 127
+    # the same tables and step draws as the float cache of the same seed
+    wf = W.small_random(3, 4, 300, 8, 2, 64)
+    assert torch.equal(wf.block_tables, wl.block_tables) and torch.equal(wf.ctx0, wl.ctx0)
+    assert torch.equal(wf.step(0).q, wl.step(0).q) and wl.step(0).k_new.dtype == torch.bfloat16
+    # bytes: D codes + a 4-byte scale per (token, head) row, for K and V
+    ctx = wl.ctx0.to(torch.int64)
+    assert wl.decode_bytes(0) == (int(ctx.sum()) * 2 * 2 * (64 + 4) + 2 * 4 * 8 * 64 * 2
+                                  + 4 * int(((ctx + 15) // 16).sum()) + 4 * 4)
