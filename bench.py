@@ -50,7 +50,8 @@ def parse():
     p.add_argument("--partition", type=int, default=0)
     p.add_argument("--workload", default=WORKLOAD,
                    help="llama3_8b_decode (the headline line) or one of tiny_fp32, llama32_1b_decode, "
-                        "prefix_shared_8k, mixed_mistral7b (per-call figures for that workload)")
+                        "prefix_shared_8k, mixed_mistral7b, llama32_1b_decode_int8, llama3_8b_decode_int8 "
+                        "(per-call figures for that workload)")
     p.add_argument("--quick", action="store_true",
                    help="no CPU baseline, no 1 s pre-warm, no end-to-end pass (for profiler runs)")
     return p.parse_args()
@@ -346,23 +347,30 @@ def run_ours(args, rank, world, local_rank):
     # e2e through the public API with host buffers: pinned H2D of the step's
     # inputs (q, new K/V, slots, context lengths, block tables), the two calls,
     # D2H of the attention output, synchronised every step
-    host_in = [(s.slot_mapping.pin_memory(), s.k_new.pin_memory(), s.v_new.pin_memory(), s.q.pin_memory(),
-                s.context_lens.pin_memory()) for s in steps_in]
-    bt_host = bt_cpu.pin_memory()
+    # e2e through the public API with host buffers: each step's inputs (new-token slots, new K/V, q,
+    # context lengths, block tables) sit packed in one pinned host buffer and go to the device in one
+    # H2D copy; then the two calls, a D2H copy of the attention output, and a synchronise
+    def pack(st):
+        parts = [st.slot_mapping, st.k_new, st.v_new, st.q, st.context_lens, bt_cpu]
+        flat = [x.contiguous().view(torch.uint8).reshape(-1) for x in parts]
+        pad = [(-f.numel()) % 16 for f in flat]   # keep every view 16-byte aligned
+        buf = torch.cat([torch.cat([f, torch.zeros(p_, dtype=torch.uint8)]) for f, p_ in zip(flat, pad)])
+        return buf.pin_memory(), [(x.dtype, tuple(x.shape), f.numel() + p_) for x, f, p_ in zip(parts, flat, pad)]
+    packed = [pack(st) for st in steps_in]
+    layout = packed[0][1]
+    d_buf = torch.empty(packed[0][0].numel(), dtype=torch.uint8, device=dev)
+    views, off = [], 0
+    for dt, shp, nb in layout:
+        n = int(torch.Size(shp).numel()) * torch.empty((), dtype=dt).element_size()
+        views.append(d_buf[off:off + n].view(dt).view(shp))
+        off += nb
+    d_slots, d_kn, d_vn, d_q, d_ctx, d_bt = views
     out_host = torch.empty((S, hq, d), dtype=wl.dtype).pin_memory()
-    d_slots, d_kn, d_vn, d_q, d_ctx = (torch.empty_like(x, device=dev) for x in host_in[0])
-    d_bt = torch.empty_like(bt_cpu, device=dev)
-    h2d = sum(x.numel() * x.element_size() for x in host_in[0]) + bt_host.numel() * bt_host.element_size()
+    h2d = packed[0][0].numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step(t):
-        hs, hk, hv, hq_, hc = host_in[t % wl.steps]
-        d_slots.copy_(hs, non_blocking=True)
-        d_kn.copy_(hk, non_blocking=True)
-        d_vn.copy_(hv, non_blocking=True)
-        d_q.copy_(hq_, non_blocking=True)
-        d_ctx.copy_(hc, non_blocking=True)
-        d_bt.copy_(bt_host, non_blocking=True)
+        d_buf.copy_(packed[t % wl.steps][0], non_blocking=True)
         pa.pa_append_kv(kp, vp, d_slots, d_kn, d_vn, stream=stream)
         pa.pa_decode_attention(out, d_q, kp, vp, d_bt, d_ctx, wl.scale, max_context_len=max_ctx,
                                partition_size=args.partition, workspace=ws, stream=stream)
@@ -431,6 +439,8 @@ def run_other(args):
     torch.cuda.set_device(dev)
     wl = W.WORKLOADS[args.workload]()
     kp, vp = wl.k_pool.to(dev), wl.v_pool.to(dev)
+    ks = wl.k_scales.to(dev) if wl.kv_int8 else None
+    vs = wl.v_scales.to(dev) if wl.kv_int8 else None
     bt = wl.decode_block_tables.contiguous().to(dev)
     pbt = wl.prefill_block_tables.contiguous().to(dev) if wl.prompt_lens else None
     steps_in = [wl.step(t) for t in range(wl.steps)]
@@ -457,20 +467,30 @@ def run_other(args):
             flush.sum()   # reads 512 MB: evicts L2 without leaving dirty lines behind
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         evs[0].record(stream)
-        pa.pa_append_kv(kp, vp, d["slots"], d["kn"], d["vn"], stream=stream)
+        if wl.kv_int8:
+            pa.pa_append_kv_int8(kp, vp, ks, vs, d["slots"], d["kn"], d["vn"], stream=stream)
+        else:
+            pa.pa_append_kv(kp, vp, d["slots"], d["kn"], d["vn"], stream=stream)
         evs[1].record(stream)
         if wl.prompt_lens:
             pa.pa_prefill_attention(d["pout"], d["qp"], kp, vp, pbt, d["cu"], d["pctx"], wl.scale,
                                     max_q_len=max(wl.prompt_lens), max_context_len=max(wl.prompt_lens),
                                     stream=stream)
         evs[2].record(stream)
-        pa.pa_decode_attention(out, d["q"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
-                               partition_size=args.partition, workspace=ws, stream=stream)
+        if wl.kv_int8:
+            pa.pa_decode_attention_int8(out, d["q"], kp, vp, ks, vs, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
+                                        partition_size=args.partition, workspace=ws, stream=stream)
+        else:
+            pa.pa_decode_attention(out, d["q"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
+                                   partition_size=args.partition, workspace=ws, stream=stream)
         evs[3].record(stream)
         return evs
     for w in range(args.warmup):
         step(w, False)
     torch.cuda.synchronize()
+    # a ~50 ms device-side delay lets the host enqueue every timed step before the GPU starts on
+    # them, so that the events time the GPU work and not the host's enqueue of small calls
+    torch.cuda._sleep(100_000_000)
     evl = [step(args.warmup + k, True) for k in range(args.steps)]
     torch.cuda.synchronize()
     for k, e in enumerate(evl):

@@ -50,7 +50,10 @@ extern "C" {
 #define PA_BLOCK_SIZE 16
 #define PA_VERSION 1
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
+/* PA_I8 is the element type of an INT8 KV cache only (pools of int8 codes with
+ * a float32 scale per row, see pa_append_kv_int8); q, out and new K/V rows are
+ * never int8. */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2, PA_I8 = 3 } pa_dtype;
 
 enum {
   PA_OK = 0,
@@ -74,7 +77,9 @@ typedef struct {
   int num_kv_heads; /* H_kv (>= 1)                                            */
   int block_size;   /* tokens per block; must be PA_BLOCK_SIZE (16)          */
   int head_dim;     /* D: 64 or 128                                           */
-  int dtype;        /* pa_dtype of pools, q, k_new/v_new and out             */
+  int dtype;        /* pa_dtype of pools, q, k_new/v_new and out; PA_I8 for  */
+                    /* an INT8 cache (the *_int8 calls; q and out then have  */
+                    /* their own act_dtype)                                  */
 } pa_pool_desc;
 
 /* Library version (PA_VERSION of the build). */
@@ -193,6 +198,65 @@ PA_API int pa_prefill_attention(void* out, const void* q, const void* k_pool, co
                          const int32_t* context_lens, float scale, int num_seqs,
                          int num_q_heads, int max_blocks_per_seq, int max_q_len,
                          int max_context_len, const pa_pool_desc* pool, void* stream);
+
+/*
+ * INT8 KV cache ("LLM Inference Server", Optional Bonus Extensions: INT8
+ * KV-Cache Quantization -- the cached K and V are quantised dynamically to
+ * int8 per token head; the quantiser is the symmetric absmax rule of its
+ * Required Mathematical Concepts: s = max|x| / 127, x_q = round(x / s),
+ * x_hat = s * x_q).
+ *
+ * Storage, with pool->dtype = PA_I8:
+ *   k_codes, v_codes   : int8    [num_blocks][H_kv][16][D]  (the float pool layout)
+ *   k_scales, v_scales : float32 [num_blocks][H_kv][16]     (one per row)
+ * Row (block, head, offset) stands for x_hat[d] = scales[row] * codes[row][d].
+ * q, out, k_new and v_new have the activation dtype `act_dtype`, PA_BF16 or
+ * PA_F16.  Pointers: codes and k_new/v_new/q/out 16-byte aligned, scales
+ * 16-byte aligned, slot_mapping 8-byte aligned.
+ */
+
+/*
+ * pa_append_kv_int8 -- quantise this step's new K/V rows into the INT8 cache.
+ *
+ * For every token t with slot = slot_mapping[t] >= 0 and every KV head h, the
+ * row x = k_new[t][h][:] (act_dtype values, widened exactly to float32) is
+ * stored as
+ *     s = max_d |x[d]| / 127                     (float32, IEEE division)
+ *     k_codes[slot/16][h][slot%16][d] = round(x[d] / s)   (IEEE division,
+ *                                                  ties to even, in [-127, 127])
+ *     k_scales[slot/16][h][slot%16]   = s
+ * and the same for V; an all-zero row stores s = 0 and zero codes.  Codes and
+ * scales are bit-exact functions of the row (every float operation is a single
+ * correctly rounded one).  A row holding Inf or NaN stores unspecified codes
+ * and a non-finite scale.  Negative slots are skipped; slots must be distinct.
+ * Errors as pa_append_kv, plus PA_ERR_INVALID when pool->dtype is not PA_I8 or
+ * act_dtype is not PA_BF16/PA_F16.
+ */
+PA_API int pa_append_kv_int8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                             const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                             int num_tokens, int act_dtype, const pa_pool_desc* pool, void* stream);
+
+/*
+ * pa_decode_attention_int8 -- pa_decode_attention over an INT8 cache.
+ *
+ * out[s][h] = softmax_i( scale * q[s][h] . K_hat_s[i][g] ) V_hat_s[i][g] with
+ * K_hat = k_scales * k_codes and V_hat = v_scales * v_codes row by row; every
+ * other rule (GQA mapping, context lengths, zero rows, split-K partitions and
+ * their merge, the workspace and its zero-fill contract, partition_size) is
+ * that of pa_decode_attention, with pool->dtype = PA_I8 in
+ * pa_decode_workspace_size / pa_decode_partition_size.  Scores, softmax and
+ * accumulation run in fp32; out (act_dtype) is rounded once.  Scale entries
+ * of positions outside the contexts are never used, whatever they hold.
+ * Errors as pa_decode_attention, plus PA_ERR_INVALID when pool->dtype is not
+ * PA_I8 or act_dtype is not PA_BF16/PA_F16.
+ */
+PA_API int pa_decode_attention_int8(void* out, const void* q, const void* k_codes,
+                                    const void* v_codes, const float* k_scales,
+                                    const float* v_scales, const int32_t* block_tables,
+                                    const int32_t* context_lens, float scale, int num_seqs,
+                                    int num_q_heads, int max_blocks_per_seq, int max_context_len,
+                                    int partition_size, int act_dtype, const pa_pool_desc* pool,
+                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of the per-device array behind pa_decode_attention_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -16,12 +16,12 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libpa.so")
 
-PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_F32, PA_BF16, PA_F16, PA_I8 = 0, 1, 2, 3
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = 0, -1, -2, -3, -4
 PA_DEV_BAD_SLOT, PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_CONTEXT, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 BLOCK_SIZE = 16
 
-_DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
+_DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16, torch.int8: PA_I8}
 
 
 class PaError(RuntimeError):
@@ -67,6 +67,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                        pdesc, vp]
     L.pa_device_status.restype = i32
     L.pa_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+    L.pa_append_kv_int8.restype = i32
+    L.pa_append_kv_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, pdesc, vp]
+    L.pa_decode_attention_int8.restype = i32
+    L.pa_decode_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
+                                           pdesc, vp, sz, vp]
     _lib = L
     return L
 
@@ -175,9 +180,10 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor
           "block_tables must be int32 [S][max_blocks]")
     _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
     L = load_library()
-    need = pa_decode_workspace_size(S, hq, max_context_len, k_pool, partition_size)
-    if workspace is None and need > 0:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:   # the library checks the size of a workspace it is given
+        need = pa_decode_workspace_size(S, hq, max_context_len, k_pool, partition_size)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.pa_decode_attention(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                                  _ptr(context_lens), float(scale), S, hq, int(block_tables.shape[1]),
@@ -245,3 +251,70 @@ def pa_decode_attention_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torc
     _check(fn(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
               float(scale), S, hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
               ctypes.byref(desc), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV cache: int8 code pools [N_blk][H_kv][16][D] + float32 scales [N_blk][H_kv][16]
+# ---------------------------------------------------------------------------
+
+def _int8_cache(k_codes, v_codes, k_scales, v_scales):
+    desc = _pools(k_codes, v_codes)
+    _need(k_codes.dtype == torch.int8, "INT8 cache code pools must be torch.int8")
+    for n, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _cuda_contig(n, t)
+        _need(t.dtype == torch.float32 and tuple(t.shape) == tuple(k_codes.shape[:3]),
+              f"{n} must be float32 {tuple(k_codes.shape[:3])}")
+    return desc
+
+
+def _act(t: torch.Tensor) -> int:
+    _need(t.dtype in (torch.bfloat16, torch.float16), "INT8 cache activations must be bf16 or fp16")
+    return _DTYPES[t.dtype]
+
+
+def pa_append_kv_int8(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch.Tensor,
+                      v_scales: torch.Tensor, slot_mapping: torch.Tensor, k_new: torch.Tensor,
+                      v_new: torch.Tensor, stream=None) -> None:
+    """Quantise k_new/v_new [T][H_kv][D] (bf16/fp16) per (token, head) row into
+    the INT8 cache at slot_mapping (int64 [T])."""
+    desc = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    for n, t in (("slot_mapping", slot_mapping), ("k_new", k_new), ("v_new", v_new)):
+        _cuda_contig(n, t)
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.dim() == 1, "slot_mapping must be int64 [T]")
+    T = slot_mapping.shape[0]
+    shape = (T, k_codes.shape[1], k_codes.shape[3])
+    _need(tuple(k_new.shape) == shape and tuple(v_new.shape) == shape, f"k_new/v_new must be {shape}")
+    _need(k_new.dtype == v_new.dtype, "k_new and v_new must share a dtype")
+    L = load_library()
+    _check(L.pa_append_kv_int8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(slot_mapping),
+                               _ptr(k_new), _ptr(v_new), int(T), _act(k_new), ctypes.byref(desc),
+                               _stream(stream)))
+
+
+def pa_decode_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                             k_scales: torch.Tensor, v_scales: torch.Tensor, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, scale: float, max_context_len: int,
+                             partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                             stream=None) -> None:
+    """pa_decode_attention over an INT8 cache; out, q: [S][H_q][D] bf16/fp16.
+    ``workspace`` as in pa_decode_attention (sized with the int8 code pool)."""
+    desc = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 3 and q.shape[2] == k_codes.shape[3], "q must be [S][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out/q shape or dtype mismatch")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
+    L = load_library()
+    if workspace is None:
+        need = pa_decode_workspace_size(S, hq, max_context_len, k_codes, partition_size)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.pa_decode_attention_int8(_ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+                                      _ptr(v_scales), _ptr(block_tables), _ptr(context_lens), float(scale), S, hq,
+                                      int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+                                      _act(q), ctypes.byref(desc), _ptr(workspace), int(ws_bytes),
+                                      _stream(stream)))

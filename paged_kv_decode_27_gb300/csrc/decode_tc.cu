@@ -20,6 +20,11 @@
 //    softmax in the log2 domain (scale folded with log2 e), P^T moved into the
 //    B-operand layout with movmatrix, and O^T += V^T P^T with V read through
 //    ldmatrix.trans.  Accumulators stay in registers.
+//  * The softmax reference is raised lazily: a warp vote finds the blocks
+//    with a score more than 2^8 above it, and only those pay for the
+//    cross-lane maximum and the rescale of the accumulators; the weights of
+//    every other block are exponentials against the current reference (<= 256,
+//    exact in the final normalisation).
 //  * The W warp states are merged in shared memory; the CTA writes the final
 //    row (one partition) or a normalised partial plus its log2-sum-exp2; the
 //    last partition of a (sequence, KV head) to finish merges them all by
@@ -33,6 +38,10 @@
 #include "pa_internal.h"
 
 namespace pa {
+
+namespace {
+constexpr float kLazy = 8.f;   // log2 headroom of the softmax reference
+}
 
 template <typename T, int D, int W, int NS>
 __global__ void __launch_bounds__(W * 32)
@@ -134,8 +143,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     }
   }
 
-  // Online-softmax state for query heads 2*tq and 2*tq+1 (log2 domain).
-  float m_run[2] = {-INFINITY, -INFINITY};
+  // Online-softmax state for query heads 2*tq and 2*tq+1 (log2 domain).  The
+  // reference m_ref is raised lazily: only when a score exceeds it by more than
+  // kLazy, so unnormalised weights stay <= 2^kLazy and most blocks need no
+  // cross-lane reduction and no rescale of the accumulators.
+  float m_ref[2] = {-INFINITY, -INFINITY};
+  float mu[2] = {0.f, 0.f};   // m_ref, or 0 while it is -inf
   float l_run[2] = {0.f, 0.f};
   float acc[KS][4];
 #pragma unroll
@@ -182,23 +195,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     float x2 = (g + 8 < nvalid) ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
     float x3 = (g + 8 < nvalid) ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
 
-    // ---- online softmax ---------------------------------------------------
-    float mb0 = warp_max_xor(fmaxf(x0, x2), 4, 16);
-    float mb1 = warp_max_xor(fmaxf(x1, x3), 4, 16);
-    const float mn0 = fmaxf(m_run[0], mb0);
-    const float mn1 = fmaxf(m_run[1], mb1);
-    const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    const float al0 = exp2f(m_run[0] - mu0);
-    const float al1 = exp2f(m_run[1] - mu1);
-    const float p0 = exp2f(x0 - mu0);
-    const float p1 = exp2f(x1 - mu1);
-    const float p2 = exp2f(x2 - mu0);
-    const float p3 = exp2f(x3 - mu1);
-    l_run[0] = l_run[0] * al0 + (p0 + p2);
-    l_run[1] = l_run[1] * al1 + (p1 + p3);
-    m_run[0] = mn0;
-    m_run[1] = mn1;
+    // ---- raise the reference (rare) -------------------------------------------
+    const bool grow = fmaxf(x0, x2) > m_ref[0] + kLazy || fmaxf(x1, x3) > m_ref[1] + kLazy;
+    if (__any_sync(0xffffffffu, grow)) {
+      const float mb0 = warp_max_xor(fmaxf(x0, x2), 4, 16);
+      const float mb1 = warp_max_xor(fmaxf(x1, x3), 4, 16);
+      const float mn0 = fmaxf(m_ref[0], mb0);
+      const float mn1 = fmaxf(m_ref[1], mb1);
+      const float nu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float nu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = fast_exp2(m_ref[0] - nu0);
+      const float al1 = fast_exp2(m_ref[1] - nu1);
+      l_run[0] *= al0;
+      l_run[1] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+      m_ref[0] = mn0;
+      m_ref[1] = mn1;
+      mu[0] = nu0;
+      mu[1] = nu1;
+    }
+    const float p0 = fast_exp2(x0 - mu[0]);
+    const float p1 = fast_exp2(x1 - mu[1]);
+    const float p2 = fast_exp2(x2 - mu[0]);
+    const float p3 = fast_exp2(x3 - mu[1]);
+    l_run[0] += p0 + p2;
+    l_run[1] += p1 + p3;
 
     // P^T as the B operand (k = token, n = head): transpose the two 8x8 halves
     const uint32_t pb0 = movmatrix_trans(Mma<T>::pack(p0, p1));
@@ -222,10 +249,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         vf[2] &= lo1 | hi1;
         vf[3] &= lo1 | hi1;
       }
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
       Mma<T>::run(acc[mt], vf, pb0, pb1);
     }
 
@@ -269,11 +292,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   }
   if (g == 0) {
     if (h0 < G) {
-      red_m[warp * 8 + h0] = m_run[0];
+      red_m[warp * 8 + h0] = m_ref[0];
       red_l[warp * 8 + h0] = l_run[0];
     }
     if (h1 < G) {
-      red_m[warp * 8 + h1] = m_run[1];
+      red_m[warp * 8 + h1] = m_ref[1];
       red_l[warp * 8 + h1] = l_run[1];
     }
   }

@@ -55,8 +55,23 @@ int elem_bytes(int dtype) {
     case PA_F32: return 4;
     case PA_BF16:
     case PA_F16: return 2;
+    case PA_I8: return 1;
     default: return 0;
   }
+}
+
+// The float entry points take float pools only; an INT8 cache has its own.
+int reject_int8(const pa_pool_desc* pool) {
+  if (pool->dtype == PA_I8)
+    return fail(PA_ERR_INVALID, "an INT8 pool (dtype PA_I8) needs the *_int8 entry points");
+  return PA_OK;
+}
+
+int check_int8(const pa_pool_desc* pool, int act_dtype) {
+  if (pool->dtype != PA_I8) return fail(PA_ERR_INVALID, "pool dtype must be PA_I8 for an INT8 cache");
+  if (act_dtype != PA_BF16 && act_dtype != PA_F16)
+    return fail(PA_ERR_INVALID, "act_dtype must be PA_BF16 or PA_F16 (got %d)", act_dtype);
+  return PA_OK;
 }
 
 int check_pool(const pa_pool_desc* pool) {
@@ -136,21 +151,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The pool viewed as a 2-D tensor of rows (block, head, offset) x head_dim,
-// loaded in boxes of 16 rows x 64 elements (128 bytes) with 128-byte swizzle.
+// The pool viewed as a 2-D tensor of rows (block, head, offset) x head_dim.
+// bf16/fp16: boxes of 16 rows x 64 elements (128 bytes), 128-byte swizzle.
+// INT8 codes: boxes of 16 whole rows (D bytes), 128-byte swizzle for D = 128
+// and 64-byte swizzle for D = 64.
 int make_pool_map(CUtensorMap* map, const void* pool_ptr, const pa_pool_desc* pool) {
   auto enc = encode_fn();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const CUtensorMapDataType dt =
-      pool->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const bool q8 = pool->dtype == PA_I8;
+  const CUtensorMapDataType dt = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                    : (pool->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(pool->head_dim),
                         static_cast<cuuint64_t>(pool->num_blocks) * pool->num_kv_heads * PA_BLOCK_SIZE};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pool->head_dim) * 2};
-  cuuint32_t box[2] = {64, PA_BLOCK_SIZE};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pool->head_dim) * elem_bytes(pool->dtype)};
+  cuuint32_t box[2] = {q8 ? static_cast<cuuint32_t>(pool->head_dim) : 64u, PA_BLOCK_SIZE};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      (q8 && pool->head_dim == 64) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = enc(map, dt, 2, const_cast<void*>(pool_ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return PA_OK;
 }
@@ -231,6 +252,7 @@ int pa_append_kv(void* k_pool, void* v_pool, const int64_t* slot_mapping, const 
   t_err.clear();
   int rc = check_pool(pool);
   if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
   if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens must be >= 0");
   if (num_tokens == 0) return PA_OK;
   if (!k_pool || !v_pool || !slot_mapping || !k_new || !v_new)
@@ -274,6 +296,7 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
   t_err.clear();
   int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool);
   if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
@@ -342,6 +365,7 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   t_err.clear();
   int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, 0, pool);
   if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
   if (pool->dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "prefill needs bf16 or fp16 pools");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
   if (max_q_len < 0 || max_q_len > max_context_len)
@@ -378,6 +402,98 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
   cudaError_t e = pa::launch_prefill_umma(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return PA_OK;
+}
+
+int pa_append_kv_int8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                      const int64_t* slot_mapping, const void* k_new, const void* v_new, int num_tokens,
+                      int act_dtype, const pa_pool_desc* pool, void* stream) {
+  t_err.clear();
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = check_int8(pool, act_dtype)) != PA_OK) return rc;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens must be >= 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!k_codes || !v_codes || !k_scales || !v_scales || !slot_mapping || !k_new || !v_new)
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales) ||
+      !aligned16(k_new) || !aligned16(v_new))
+    return fail(PA_ERR_INVALID, "codes, scales and k_new/v_new must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+    return fail(PA_ERR_INVALID, "slot_mapping must be 8-byte aligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  cudaError_t e = pa::launch_append_q8(k_codes, v_codes, k_scales, v_scales, slot_mapping, k_new, v_new,
+                                       num_tokens, pool->num_kv_heads, pool->head_dim, act_dtype,
+                                       pool->num_blocks, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append_kv_int8 launch");
+  return PA_OK;
+}
+
+int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                             const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, int num_seqs, int num_q_heads,
+                             int max_blocks_per_seq, int max_context_len, int partition_size, int act_dtype,
+                             const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = check_int8(pool, act_dtype)) != PA_OK) return rc;
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_codes || !v_codes || !k_scales || !v_scales || !context_lens ||
+      (max_blocks_per_seq > 0 && !block_tables))
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) ||
+      !aligned16(v_scales))
+    return fail(PA_ERR_INVALID, "out, q, codes and scales must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "block_tables and context_lens must be 4-byte aligned");
+
+  const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int part_blocks = part / PA_BLOCK_SIZE;
+  const int max_splits = max_splits_for(max_context_len, part_blocks);
+  const WsLayout ws = ws_layout(num_seqs, num_q_heads, max_splits, pool->head_dim);
+  if (ws.total > 0 && static_cast<long long>(num_seqs) * pool->num_kv_heads > kMaxCounters)
+    return fail(PA_ERR_UNSUPPORTED, "split-K over more than %d (sequence, KV head) pairs in one call",
+                kMaxCounters);
+  if (ws.total > 0) {
+    if (!workspace) return fail(PA_ERR_INVALID, "workspace of %zu bytes required, got NULL", ws.total);
+    if (workspace_bytes < ws.total)
+      return fail(PA_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, ws.total);
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+  }
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+
+  pa::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_pool = k_codes;
+  a.v_pool = v_codes;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.head_dim = pool->head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.num_blocks = pool->num_blocks;
+  a.part_blocks = part_blocks;
+  a.max_splits = max_splits;
+  a.ws_count = ws.total ? static_cast<int*>(workspace) : nullptr;
+  a.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_off) : nullptr;
+  a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
+  a.status = status;
+  CUtensorMap kmap, vmap;
+  if ((rc = pool_map(&kmap, k_codes, pool)) != PA_OK) return rc;
+  if ((rc = pool_map(&vmap, v_codes, pool)) != PA_OK) return rc;
+  cudaError_t e = pa::launch_decode_q8(a, act_dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode_int8 launch");
   return PA_OK;
 }
 

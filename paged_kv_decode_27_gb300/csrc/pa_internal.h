@@ -31,6 +31,8 @@ struct DecodeArgs {
   float* ws_lse;           // [S][H_q][max_splits]     partial log2-sum-exp2
   int* ws_count;           // [S][H_kv] partitions finished (zero between calls)
   int* status;             // device status word (PA_DEV_* bits)
+  const float* k_scales;   // INT8 cache only: [N_blk][H_kv][16] row scales
+  const float* v_scales;
 };
 
 struct PrefillArgs {
@@ -64,6 +66,15 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int dtype, const CUtensorMap& 
 
 // CUDA-core decode (any supported dtype; the fp32 path).
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t stream);
+
+// INT8 cache: quantise-on-append of bf16/fp16 rows (act_dtype), and decode
+// over int8 codes with float32 row scales (q / out in act_dtype).
+cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                             const int64_t* slot_mapping, const void* k_new, const void* v_new, int num_tokens,
+                             int num_kv_heads, int head_dim, int act_dtype, int num_blocks, int* status,
+                             cudaStream_t stream);
+cudaError_t launch_decode_q8(const DecodeArgs& a, int act_dtype, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, cudaStream_t stream);
 
 // Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).
 cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,

@@ -131,3 +131,42 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         B.load_library(str(tmp_path / "nope.so"))
+
+
+def _decode8(lib, desc, act=B.PA_BF16, ks=FAKE, out=FAKE, maxc=100, part=512, S=4):
+    f = ctypes.c_void_p(FAKE)
+    return lib.pa_decode_attention_int8(ctypes.c_void_p(out), f, f, f, ctypes.c_void_p(ks), f, f, f, 0.125, S, 32,
+                                        8, maxc, part, act, ctypes.byref(desc), None, 0, None)
+
+
+def test_int8_cache_entry_points_validate_on_the_host(lib):
+    i8 = _desc(dt=B.PA_I8)
+    # the float calls refuse an INT8 pool, the INT8 calls refuse a float pool
+    assert _decode(lib, i8) == B.PA_ERR_INVALID and "int8" in B.pa_last_error()
+    assert _decode8(lib, _desc(dt=B.PA_BF16)) == B.PA_ERR_INVALID
+    assert _decode8(lib, i8, act=B.PA_F32) == B.PA_ERR_INVALID
+    assert _decode8(lib, i8, act=B.PA_I8) == B.PA_ERR_INVALID
+    assert _decode8(lib, i8, ks=0) == B.PA_ERR_INVALID
+    assert _decode8(lib, i8, ks=FAKE + 4) == B.PA_ERR_INVALID        # scales misaligned
+    assert _decode8(lib, _desc(d=96, dt=B.PA_I8)) == B.PA_ERR_UNSUPPORTED
+    assert _decode8(lib, i8, S=0) == B.PA_OK
+    f = ctypes.c_void_p(FAKE)
+    app = lambda desc=i8, act=B.PA_BF16, T=4, ks=f: lib.pa_append_kv_int8(f, f, ks, f, f, f, f, T, act,
+                                                                          ctypes.byref(desc), None)
+    assert app(desc=_desc()) == B.PA_ERR_INVALID
+    assert app(act=B.PA_F32) == B.PA_ERR_INVALID
+    assert app(ks=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
+    assert app(T=-1) == B.PA_ERR_INVALID
+    assert app(T=0) == B.PA_OK
+    fl = ctypes.c_void_p(FAKE)
+    assert lib.pa_append_kv(fl, fl, fl, fl, fl, 4, ctypes.byref(i8), None) == B.PA_ERR_INVALID
+    # the workspace of an INT8 cache has the float formula (partials are fp32)
+    assert lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(_desc(d=128, dt=B.PA_I8))) == \
+        lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(_desc(d=128)))
+
+
+def test_int8_without_gpu_is_a_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _decode8(lib, _desc(dt=B.PA_I8)) == B.PA_ERR_CUDA

@@ -1,0 +1,256 @@
+"""INT8 KV cache on the GPU against the float64 oracle.
+
+Append: codes and scales bit-exact (the quantiser's float32 decisions are
+single IEEE operations on both sides).  Decode: the output against the oracle's
+attention over the dequantised cache, |gpu - ref| <= 2e-2 + 1e-2 |ref| (fp32
+accumulation inside, one rounding of the bf16/fp16 output)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_27_gb300 import binding as pa
+from paged_kv_decode_27_gb300 import workloads as W
+from _util import assert_close_to_ref, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class Cache:
+    """Device copy of a workload's INT8 cache plus the oracle's host state."""
+
+    def __init__(self, wl: W.Workload):
+        self.kc, self.vc = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+        self.ks, self.vs = wl.k_scales.to(DEV), wl.v_scales.to(DEV)
+        self.host = [to_np(wl.k_pool), to_np(wl.v_pool), wl.k_scales.numpy().copy(), wl.v_scales.numpy().copy()]
+
+    def append(self, st: W.StepInputs):
+        pa.pa_append_kv_int8(self.kc, self.vc, self.ks, self.vs, st.slot_mapping.to(DEV), st.k_new.to(DEV),
+                             st.v_new.to(DEV))
+        self.host = list(oracle.append_int8_ref(*self.host, st.slot_mapping.numpy(), to_np(st.k_new),
+                                                to_np(st.v_new)))
+
+    def decode(self, wl, st, part=0, max_ctx=None):
+        out = torch.empty(st.q.shape, dtype=st.q.dtype, device=DEV)
+        mc = int(st.context_lens.max()) if max_ctx is None else max_ctx
+        pa.pa_decode_attention_int8(out, st.q.to(DEV), self.kc, self.vc, self.ks, self.vs,
+                                    wl.decode_block_tables.contiguous().to(DEV), st.context_lens.to(DEV), wl.scale,
+                                    max_context_len=mc, partition_size=part)
+        torch.cuda.synchronize()
+        return out
+
+    def ref(self, wl, st, seqs=None):
+        return oracle.decode_int8_ref(to_np(st.q), *self.host, wl.decode_block_tables.contiguous().numpy(),
+                                      st.context_lens.numpy(), wl.scale, seqs=seqs)
+
+    def same_as_oracle(self):
+        torch.cuda.synchronize()
+        got = [to_np(self.kc), to_np(self.vc), self.ks.cpu().numpy(), self.vs.cpu().numpy()]
+        return all(np.array_equal(g.view(np.uint8), h.view(np.uint8)) for g, h in zip(got, self.host))
+
+
+def _check(wl, st, cache, parts=(0,), seqs=None):
+    ref = cache.ref(wl, st, seqs=seqs)
+    for part in parts:
+        out = cache.decode(wl, st, part)
+        idx = list(range(out.shape[0])) if seqs is None else list(seqs)
+        assert_close_to_ref(out[idx], ref[idx], wl.dtype, f"{wl.name} int8 partition={part}")
+    assert pa.pa_device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# append: quantise on write
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.bfloat16), (128, torch.float16),
+                                     (64, torch.float16)])
+def test_append_int8_bit_exact(d, dtype):
+    wl = W.small_random(60 + d, 6, 300, 16, 4, d, dtype, kv="int8")
+    st = wl.step(0)
+    cache = Cache(wl)
+    cache.append(st)
+    assert cache.same_as_oracle()
+    assert pa.pa_device_status() == 0
+
+
+def test_append_int8_special_rows():
+    """Zero rows, exact ties (x / s = k + 1/2 with s exact), a single nonzero,
+    tiny (subnormal scale) and huge magnitudes, padding and out-of-range slots."""
+    hkv, d, T = 2, 128, 8
+    g = torch.Generator().manual_seed(61)
+    nb = 4
+    kc = torch.randint(-127, 128, (nb, hkv, 16, d), generator=g, dtype=torch.int16).to(torch.int8)
+    vc = kc.clone()
+    ks = torch.full((nb, hkv, 16), 7.0)
+    vs = ks.clone()
+    x = torch.randn((T, hkv, d), generator=g)
+    x[0] = 0.0
+    x[1, 0] = 127.0
+    x[1, 0, 1:] = torch.arange(1, d, dtype=torch.float32) * 0.5 - 32.0    # many .5 ties with s = 1
+    x[2] = 0.0
+    x[2, 1, 5] = -3.0
+    x[3] *= 1e-38                                                     # scale underflows to a subnormal
+    x[4] *= 3e4
+    xk = x.to(torch.bfloat16)
+    xv = (x * 0.5).to(torch.bfloat16)
+    slots = torch.tensor([0, 17, 33, 50, 63, -1, 5, 40], dtype=torch.int64)
+    wl = W.Workload(name="special", config_id=0, dtype=torch.bfloat16, num_q_heads=2, num_kv_heads=hkv,
+                    head_dim=d, scale=0.1, steps=1, k_pool=kc, v_pool=vc,
+                    block_tables=torch.zeros((1, 1), dtype=torch.int32), ctx0=torch.zeros(1, dtype=torch.int32),
+                    decode_rows=slice(0, 1), k_scales=ks, v_scales=vs)
+    cache = Cache(wl)
+    st = W.StepInputs(slot_mapping=slots, k_new=xk, v_new=xv, q=torch.zeros((1, 2, d), dtype=torch.bfloat16),
+                      context_lens=torch.zeros(1, dtype=torch.int32))
+    cache.append(st)
+    assert cache.same_as_oracle()
+    assert pa.pa_device_status() == 0
+    # a slot past the pool is skipped and reported
+    bad = slots.clone()
+    bad[2] = nb * 16 + 1
+    pa.pa_append_kv_int8(cache.kc, cache.vc, cache.ks, cache.vs, bad.to(DEV), xk.to(DEV), xv.to(DEV))
+    assert pa.pa_device_status() & pa.PA_DEV_BAD_SLOT
+
+
+def test_append_int8_llama3_8b_steps():
+    wl = W.llama3_8b_decode(steps=3, kv="int8")
+    cache = Cache(wl)
+    for t in range(3):
+        cache.append(wl.step(t))
+    assert cache.same_as_oracle()
+
+
+# ---------------------------------------------------------------------------
+# decode over the dequantised cache
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [
+    (32, 8, 128, torch.bfloat16), (8, 8, 128, torch.bfloat16), (16, 2, 128, torch.float16),
+    (32, 8, 64, torch.bfloat16), (12, 4, 64, torch.float16), (8, 1, 64, torch.bfloat16)])
+def test_decode_int8_group_sizes_dims_dtypes(hq, hkv, d, dtype):
+    wl = W.small_random(70 + hq + d, 5, 700, hq, hkv, d, dtype, kv="int8")
+    st = wl.step(0)
+    cache = Cache(wl)
+    cache.append(st)
+    _check(wl, st, cache, parts=(0, 16, 64, 512))
+
+
+@pytest.mark.parametrize("ctx", [[1, 15, 16, 17, 31, 32, 33], [63, 64, 65, 127, 128, 129, 255, 256, 257]])
+@pytest.mark.parametrize("part", [0, 16, 128])
+def test_decode_int8_ragged_boundaries(ctx, part):
+    wl = W.small_random(81, len(ctx), 0, 32, 8, 128, torch.bfloat16, ctx=ctx, kv="int8")
+    st = wl.step(0)
+    cache = Cache(wl)
+    cache.append(st)
+    _check(wl, st, cache, parts=(part,))
+
+
+def test_decode_int8_stale_slots_never_leak():
+    """Scales of every slot outside the contexts are NaN and their codes are
+    +-127: none of it may reach the output."""
+    wl = W.small_random(82, 6, 200, 16, 4, 128, torch.bfloat16, kv="int8")
+    st = wl.step(0)
+    used = set()
+    bt = wl.block_tables
+    for s in range(bt.shape[0]):
+        for p in range(int(st.context_lens[s])):
+            used.add(int(bt[s, p // 16]) * 16 + p % 16)
+    for slot in range(wl.num_blocks * 16):
+        if slot not in used:
+            b, o = divmod(slot, 16)
+            wl.k_scales[b, :, o] = float("nan")
+            wl.v_scales[b, :, o] = float("nan")
+            wl.k_pool[b, :, o] = 127
+            wl.v_pool[b, :, o] = -127
+    cache = Cache(wl)
+    cache.append(st)
+    ref = cache.ref(wl, st)
+    assert np.isfinite(ref).all()
+    for part in (0, 16, 48):
+        out = cache.decode(wl, st, part)
+        assert torch.isfinite(out.float()).all()
+        assert_close_to_ref(out, ref, wl.dtype, f"int8 stale slots part={part}")
+
+
+def test_decode_int8_zero_context_rows_are_zero():
+    wl = W.small_random(83, 4, 0, 8, 2, 128, torch.bfloat16, ctx=[50, 0, 300, 0], kv="int8")
+    st = wl.step(0)
+    cache = Cache(wl)
+    cache.append(st)
+    for part in (0, 16):
+        out = cache.decode(wl, st, part)
+        assert int(out[1].count_nonzero()) == 0 and int(out[3].count_nonzero()) == 0
+    _check(wl, st, cache, parts=(0, 16))
+
+
+@pytest.mark.parametrize("kscale,vscale,qscale", [(1e-6, 1e-6, 1.0), (300.0, 1e4, 1.0), (0.02, 0.02, 1e3),
+                                                  (0.02, 0.02, 1e-3)])
+def test_decode_int8_value_ranges(kscale, vscale, qscale):
+    """Scales and query magnitudes far from 1: the fp16 operands inside must
+    neither overflow nor lose the small rows."""
+    wl = W.small_random(84, 4, 600, 16, 4, 128, torch.bfloat16, kv="int8")
+    wl.k_scales.mul_(kscale * 127 / 3)
+    wl.v_scales.mul_(vscale * 127 / 3)
+    st = wl.step(0)
+    st.q = (st.q.float() * qscale).to(torch.bfloat16)
+    st.slot_mapping[:] = -1          # keep the drawn cache as it is
+    cache = Cache(wl)
+    ref = cache.ref(wl, st)
+    for part in (0, 64):
+        out = cache.decode(wl, st, part)
+        # the bar is relative to the output's own magnitude
+        mag = max(float(np.max(np.abs(ref))), 1e-30)
+        err = float(torch.max(torch.abs(out.double().cpu() - torch.from_numpy(ref))))
+        assert err <= 1e-2 * mag + 2e-2 * min(mag, 1.0), (err, mag)
+
+
+def test_decode_int8_llama3_8b_full_size_sampled():
+    """The batch-64, D=128 workload over an INT8 cache in the launch
+    configuration the benchmark times (automatic partition), two steps with
+    the quantising append before each, oracle on sampled sequences."""
+    wl = W.llama3_8b_decode(steps=2, kv="int8")
+    order = torch.argsort(wl.ctx0)
+    pick = sorted(set([int(order[0]), int(order[-1])] + list(range(0, 64, 9))))
+    cache = Cache(wl)
+    for t in range(2):
+        st = wl.step(t)
+        cache.append(st)
+        _check(wl, st, cache, parts=(0,), seqs=pick)
+
+
+def test_decode_int8_llama32_1b():
+    wl = W.llama32_1b_decode(steps=2, kv="int8")
+    cache = Cache(wl)
+    for t in range(2):
+        st = wl.step(t)
+        cache.append(st)
+        _check(wl, st, cache, parts=(0, 256))
+
+
+def test_int8_cache_tracks_the_float_cache():
+    """End to end: the same bf16 rows appended into a float cache and into an
+    INT8 cache give decode outputs within the quantisation error of each
+    other (|dv| <= s_v / 2 per element moves the output by at most that)."""
+    wl = W.small_random(85, 4, 0, 16, 4, 128, torch.bfloat16, ctx=[40, 100, 250, 16])
+    wq = W.small_random(85, 4, 0, 16, 4, 128, torch.bfloat16, ctx=[40, 100, 250, 16], kv="int8")
+    # write every context position of both caches from the same bf16 rows
+    g = torch.Generator().manual_seed(86)
+    bt = wl.decode_block_tables
+    slots = torch.cat([bt[s, torch.arange(c) // 16].to(torch.int64) * 16 + torch.arange(c) % 16
+                       for s, c in enumerate([40, 100, 250, 16])])
+    kn = (torch.randn((slots.numel(), 4, 128), generator=g) * 0.1).to(torch.bfloat16)
+    vn = torch.randn((slots.numel(), 4, 128), generator=g).to(torch.bfloat16)
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    pa.pa_append_kv(kp, vp, slots.to(DEV), kn.to(DEV), vn.to(DEV))
+    cache = Cache(wq)
+    st = W.StepInputs(slot_mapping=slots, k_new=kn, v_new=vn, q=wl.step(0).q,
+                      context_lens=torch.tensor([40, 100, 250, 16], dtype=torch.int32))
+    cache.append(st)
+    out_f = torch.empty(st.q.shape, dtype=torch.bfloat16, device=DEV)
+    pa.pa_decode_attention(out_f, st.q.to(DEV), kp, vp, bt.contiguous().to(DEV), st.context_lens.to(DEV), wl.scale,
+                           max_context_len=250)
+    out_q = cache.decode(wq, st)
+    smax = float(cache.vs.max())
+    assert float(torch.max(torch.abs(out_f.float() - out_q.float()))) <= smax + 0.05
