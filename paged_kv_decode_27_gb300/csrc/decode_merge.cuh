@@ -65,24 +65,38 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
   __syncthreads();
   if (!s_last) return;
   T* out = static_cast<T*>(a.out);
+  constexpr int kBatch = 8;   // partials whose loads are in flight together
   for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
     const int h = idx / D;
     const int d = idx - h * D;
     const int hq = kvh * G + h;
     const size_t row0 = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.max_splits;
-    // one pass with a running max: loads of different partitions are independent
+    // a running max over batches of partitions; each batch issues all of its
+    // loads before any arithmetic, so the merge costs ~one memory latency per
+    // batch instead of one per partition
     float M = -INFINITY, L = 0.f, O = 0.f;
-#pragma unroll 4
-    for (int p = 0; p < n_splits; ++p) {
-      const float lp = __ldcg(a.ws_lse + row0 + p);
-      const float op = __ldcg(a.ws_o + (row0 + p) * D + d);
-      if (lp == -INFINITY) continue;
-      const float mn = fmaxf(M, lp);
-      const float r = exp2f(M - mn);      // 0 while M is still -inf
-      const float w = exp2f(lp - mn);
-      L = fmaf(L, r, w);
-      O = fmaf(O, r, w * op);
-      M = mn;
+    for (int p0 = 0; p0 < n_splits; p0 += kBatch) {
+      float lp[kBatch], op[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const bool in = p0 + k < n_splits;
+        lp[k] = in ? __ldcg(a.ws_lse + row0 + p0 + k) : -INFINITY;
+        op[k] = in ? __ldcg(a.ws_o + (row0 + p0 + k) * D + d) : 0.f;
+      }
+      float mb = M;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, lp[k]);
+      if (mb == -INFINITY) continue;
+      const float r = exp2f(M - mb);      // 0 while M is still -inf
+      L *= r;
+      O *= r;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float w = exp2f(lp[k] - mb);   // 0 for empty partitions
+        L += w;
+        O = fmaf(w, op[k], O);
+      }
+      M = mb;
     }
     out[(static_cast<size_t>(s) * a.num_q_heads + hq) * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
   }

@@ -23,9 +23,10 @@ __device__ int g_pa_status = 0;
 namespace {
 
 constexpr int kGb300Sms = 152;
-// Split-K partitions are shrunk until a batch yields at least this many
-// (sequence, KV head, partition) units, i.e. several CTAs per SM.
-constexpr long long kTargetUnits = 4LL * kGb300Sms;
+// Decode CTAs resident at once (3 per SM), and the smallest partition the
+// automatic choice uses: below it the split-K merge costs more than it hides.
+constexpr long long kWaveUnits = 3LL * kGb300Sms;
+constexpr int kMinPartition = 256;
 constexpr int kMaxPartition = 2048;   // 32 blocks per warp of a 4-warp CTA
 // Split-K completion counters occupy a fixed region at the start of the
 // workspace, so no shape's partials ever overlap another shape's counters.
@@ -104,13 +105,16 @@ int* status_ptr() {
 
 int choose_partition(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
   if (requested > 0) return requested;
-  int p = 1024;
-  while (p > 64) {
-    const long long units =
-        static_cast<long long>(num_seqs) * num_kv_heads * ((max_context_len + p - 1) / p);
-    if (units >= kTargetUnits) break;
-    p /= 2;
-  }
+  // One resident wave when the batch allows it: the largest partition count
+  // (smallest partition, not below kMinPartition) whose (sequence, KV head,
+  // partition) units all fit on the GPU at once.  Past that the decode runs in
+  // several waves of 1024-token partitions.
+  const auto units = [&](int p) {
+    return static_cast<long long>(num_seqs) * num_kv_heads * ((max_context_len + p - 1) / p);
+  };
+  if (units(kMaxPartition) > kWaveUnits) return 1024;
+  int p = kMaxPartition;
+  while (p > kMinPartition && units(p / 2) <= kWaveUnits) p /= 2;
   return p;
 }
 

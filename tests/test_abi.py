@@ -113,8 +113,13 @@ def test_workspace_size_and_partition(lib):
     rows = 64 * 32 * 9
     o_end = 256 * 1024 + rows * 128 * 4          # counters, then partial outputs
     assert n == ((o_end + 255) // 256) * 256 + rows * 4
-    # few units: the partition shrinks (8 sequences of <= 2063 tokens -> 128)
-    assert lib.pa_decode_partition_size(8, 2063, 0, ctypes.byref(_desc(d=64))) == 128
+    # a batch that fits one resident wave (456 units) takes the smallest
+    # partition that still fits: 8 x 8 pairs of <= 2063 tokens -> 512 (320 units)
+    assert lib.pa_decode_partition_size(8, 2063, 0, ctypes.byref(_desc(d=64))) == 512
+    # 8 x 8 pairs of 8192 tokens: 2048 (256 units; 1024 would need 512)
+    assert lib.pa_decode_partition_size(8, 8192, 0, ctypes.byref(d)) == 2048
+    # tiny batches stop at 256 tokens
+    assert lib.pa_decode_partition_size(2, 40, 0, ctypes.byref(_desc(hkv=2, d=64))) == 256
     # one partition covers everything: no workspace
     assert lib.pa_decode_workspace_size(4, 32, 512, 512, ctypes.byref(d)) == 0
     assert lib.pa_decode_partition_size(4, 512, 256, ctypes.byref(d)) == 256
