@@ -50,8 +50,8 @@ def parse():
     p.add_argument("--partition", type=int, default=0)
     p.add_argument("--workload", default=WORKLOAD,
                    help="llama3_8b_decode (the headline line) or one of tiny_fp32, llama32_1b_decode, "
-                        "prefix_shared_8k, mixed_mistral7b, llama32_1b_decode_int8, llama3_8b_decode_int8 "
-                        "(per-call figures for that workload)")
+                        "prefix_shared_8k, mixed_mistral7b, llama32_1b_decode_int8, llama3_8b_decode_int8, "
+                        "llama3_8b_verify (per-call figures for that workload)")
     p.add_argument("--quick", action="store_true",
                    help="no CPU baseline, no 1 s pre-warm, no end-to-end pass (for profiler runs)")
     return p.parse_args()
@@ -457,6 +457,13 @@ def run_other(args):
     ws = torch.zeros(max(1, pa.pa_decode_workspace_size(S, hq, max_ctx, kp, args.partition)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((S, hq, dh), dtype=wl.dtype, device=dev)
+    vq = wl.extra.get("verify_q_len", 0)
+    if vq:   # a verification pass replaces the decode: q_len query rows per sequence
+        for t, d in enumerate(d_in):
+            d["vq"] = wl.verify_queries(t, vq).to(dev)
+        out = torch.empty((S, vq, hq, dh), dtype=wl.dtype, device=dev)
+        ws = torch.zeros(max(1, pa.pa_verify_workspace_size(S, vq, hq, max_ctx, kp, args.partition)),
+                         dtype=torch.uint8, device=dev)
     flush = torch.ones(256 << 20, dtype=torch.float16, device=dev)   # 512 MB, read to evict L2
     stream = torch.cuda.current_stream()
     rec = {"append": [], "prefill": [], "decode": []}
@@ -477,7 +484,10 @@ def run_other(args):
                                     max_q_len=max(wl.prompt_lens), max_context_len=max(wl.prompt_lens),
                                     stream=stream)
         evs[2].record(stream)
-        if wl.kv_int8:
+        if vq:
+            pa.pa_verify_attention(out, d["vq"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
+                                   partition_size=args.partition, workspace=ws, stream=stream)
+        elif wl.kv_int8:
             pa.pa_decode_attention_int8(out, d["q"], kp, vp, ks, vs, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
                                         partition_size=args.partition, workspace=ws, stream=stream)
         else:
@@ -499,7 +509,7 @@ def run_other(args):
         rec["decode"].append(e[2].elapsed_time(e[3]) * 1e3)
     med = {k: statistics.median(v) for k, v in rec.items()}
     t_mid = (args.warmup + args.steps // 2) % wl.steps
-    dec_b = wl.decode_bytes(t_mid)
+    dec_b = wl.verify_bytes(t_mid, vq) if vq else wl.decode_bytes(t_mid)
     peak, kind = peak_hbm()
     line = {"workload": wl.name, "description": wl.description, "steps": args.steps, "warmup": args.warmup,
             "l2": "evicted before every step (a 512 MB read)",

@@ -174,6 +174,34 @@ PA_API int pa_decode_attention(void* out, const void* q, const void* k_pool, con
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_verify_attention -- attention for the verification pass of speculative
+ * decoding: q_len query tokens per sequence (the last accepted token and the
+ * q_len - 1 drafted ones, "LLM Inference Server", Batched Scheduling &
+ * Speculative Decoding: the target model checks K = 4 drafted tokens in one
+ * forward pass, so q_len = K + 1 = 5), all already appended to the pool.
+ * Query i of sequence s sits at position p = context_lens[s] - q_len + i and
+ * attends keys 0..p (causal), exactly as a prompt pass over a cached prefix
+ * would; q_len = 1 is pa_decode_attention.  The K/V blocks are read once for
+ * all q_len x G query rows of a KV head, and long contexts are split into
+ * partitions merged by log-sum-exp as in pa_decode_attention.
+ *
+ *   out, q        : [num_seqs][q_len][num_q_heads][D], bf16 or fp16 pools
+ *   context_lens  : int32 [num_seqs], each >= q_len (rows whose position is
+ *                   negative see no key and are zero)
+ *   workspace     : >= pa_verify_workspace_size(...) bytes, with the zero-fill
+ *                   contract of pa_decode_attention
+ * Errors as pa_decode_attention, plus PA_ERR_INVALID for q_len < 1 and
+ * PA_ERR_UNSUPPORTED for fp32 pools or (num_q_heads/num_kv_heads) * q_len > 32.
+ */
+PA_API size_t pa_verify_workspace_size(int num_seqs, int q_len, int num_q_heads, int max_context_len,
+                                       int partition_size, const pa_pool_desc* pool);
+PA_API int pa_verify_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const int32_t* context_lens, float scale,
+                               int num_seqs, int q_len, int num_q_heads, int max_blocks_per_seq,
+                               int max_context_len, int partition_size, const pa_pool_desc* pool,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_prefill_attention -- the causal prompt pass over the same pool.
  *
  * Prefill processes all prompt tokens at once (q_len = prompt length,

@@ -205,5 +205,6 @@ def prefill_ref(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
             if want is not None and (lo + i) not in want:
                 continue
             pos = c - n + i
-            out[lo + i] = attend(q64[lo + i], k, v, scale, pos + 1)
+            # a query before the first cached position sees no key: zero row
+            out[lo + i] = attend(q64[lo + i], k, v, scale, max(pos + 1, 0))
     return out

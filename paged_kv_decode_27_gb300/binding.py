@@ -67,6 +67,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                        pdesc, vp]
     L.pa_device_status.restype = i32
     L.pa_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+    L.pa_verify_workspace_size.restype = sz
+    L.pa_verify_workspace_size.argtypes = [i32, i32, i32, i32, i32, pdesc]
+    L.pa_verify_attention.restype = i32
+    L.pa_verify_attention.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32, pdesc, vp, sz,
+                                      vp]
     L.pa_append_kv_int8.restype = i32
     L.pa_append_kv_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, pdesc, vp]
     L.pa_decode_attention_int8.restype = i32
@@ -189,6 +194,45 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor
                                  _ptr(context_lens), float(scale), S, hq, int(block_tables.shape[1]),
                                  int(max_context_len), int(partition_size), ctypes.byref(desc),
                                  _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def pa_verify_workspace_size(num_seqs: int, q_len: int, num_q_heads: int, max_context_len: int,
+                             k_pool: torch.Tensor, partition_size: int = 0) -> int:
+    L = load_library()
+    desc = pool_desc(k_pool)
+    n = L.pa_verify_workspace_size(int(num_seqs), int(q_len), int(num_q_heads), int(max_context_len),
+                                   int(partition_size), ctypes.byref(desc))
+    msg = pa_last_error()
+    if msg:
+        raise PaError(PA_ERR_INVALID, msg)
+    return int(n)
+
+
+def pa_verify_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                        block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                        max_context_len: int, partition_size: int = 0,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """out, q: [S][q_len][H_q][D]: the last q_len positions of each sequence
+    (already appended), each attending causally to the cache."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 4 and q.shape[3] == k_pool.shape[3], "q must be [S][q_len][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype == k_pool.dtype, "out/q shape or dtype mismatch")
+    S, ql, hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
+    L = load_library()
+    if workspace is None:
+        need = pa_verify_workspace_size(S, ql, hq, max_context_len, k_pool, partition_size)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.pa_verify_attention(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                 _ptr(context_lens), float(scale), S, ql, hq, int(block_tables.shape[1]),
+                                 int(max_context_len), int(partition_size), ctypes.byref(desc), _ptr(workspace),
+                                 int(ws_bytes), _stream(stream)))
 
 
 def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

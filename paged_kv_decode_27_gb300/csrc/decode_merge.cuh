@@ -3,10 +3,14 @@
 // for split-K, the CTA that finishes last for its (sequence, KV head) then
 // merges all partials (the log-sum-exp combine, fused into the decode kernel).
 //
-// Each warp leaves, for every query head h of the group (h < G <= 8):
-//   red_m[w][h]  running max of the log2-domain scores,
-//   red_l[w][h]  sum of 2^(x - m) over the warp's tokens,
-//   red_o[w][h][d] sum of 2^(x - m) * v[d].
+// A CTA works on one (sequence, KV head) and its query columns: the G query
+// heads of the group at each of the a.q_len query positions (q_len = 1 for
+// decode), column c = i * G + h for position i and head h.  Each warp leaves,
+// for every column c < G * q_len (stride NC per warp):
+//   red_m[w][c]  reference of the log2-domain scores (the running maximum, or
+//                a lazily raised value below it),
+//   red_l[w][c]  sum of 2^(x - m) over the warp's tokens,
+//   red_o[w][c][d] sum of 2^(x - m) * v[d].
 // A warp that saw no token has m = -inf, l = 0, o = 0 and weighs nothing.
 #pragma once
 
@@ -15,34 +19,44 @@
 
 namespace pa {
 
-template <typename T, int W, int D>
+// Row of q / out (and, times max_splits, of the split-K partials) that holds
+// query column c of (sequence s, KV head kvh): q and out are
+// [num_seqs][q_len][num_q_heads][D].
+__device__ __forceinline__ size_t query_row(const DecodeArgs& a, int s, int kvh, int G, int c) {
+  const int i = c / G;
+  const int h = c - i * G;
+  return (static_cast<size_t>(s) * a.q_len + i) * a.num_q_heads + kvh * G + h;
+}
+
+template <typename T, int W, int D, int NC = 8>
 __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float* red_o,
                                                 const float* red_m, const float* red_l, int G,
                                                 int s, int kvh, int split, int n_splits) {
   __shared__ int s_last;
-  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-    const int h = idx / D;
-    const int d = idx - h * D;
+  const int ncols = G * a.q_len;
+  for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+    const int c = idx / D;
+    const int d = idx - c * D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[w * NC + c]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < W; ++w) {
-        const float mw = red_m[w * 8 + h];
+        const float mw = red_m[w * NC + c];
         const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        L += f * red_l[w * 8 + h];
-        O += f * red_o[(w * 8 + h) * D + d];
+        L += f * red_l[w * NC + c];
+        O += f * red_o[(w * NC + c) * D + d];
       }
     }
-    const int hq = kvh * G + h;
+    const size_t qr = query_row(a, s, kvh, G, c);
     const float o = (L > 0.f) ? O / L : 0.f;
     if (n_splits == 1) {
       T* out = static_cast<T*>(a.out);
-      out[(static_cast<size_t>(s) * a.num_q_heads + hq) * D + d] = Elem<T>::from_f(o);
+      out[qr * D + d] = Elem<T>::from_f(o);
     } else {
-      const size_t row = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.max_splits + split;
+      const size_t row = qr * a.max_splits + split;
       a.ws_o[row * D + d] = o;
       if (d == 0) a.ws_lse[row] = (L > 0.f) ? M + log2f(L) : -INFINITY;
     }
@@ -66,11 +80,11 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
   if (!s_last) return;
   T* out = static_cast<T*>(a.out);
   constexpr int kBatch = 8;   // partials whose loads are in flight together
-  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    const int hq = kvh * G + h;
-    const size_t row0 = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.max_splits;
+  for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+    const int c = idx / D;
+    const int d = idx - c * D;
+    const size_t qr = query_row(a, s, kvh, G, c);
+    const size_t row0 = qr * a.max_splits;
     // a running max over batches of partitions; each batch issues all of its
     // loads before any arithmetic, so the merge costs ~one memory latency per
     // batch instead of one per partition
@@ -98,21 +112,21 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
       }
       M = mb;
     }
-    out[(static_cast<size_t>(s) * a.num_q_heads + hq) * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
+    out[qr * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
   }
   // leave the counter at zero for the next call on this workspace
   if (threadIdx.x == 0) *counter = 0;
 }
 
-// A sequence with an empty context produces zero rows for its heads.
+// A sequence with an empty context produces zero rows for its query columns.
 template <typename T, int D>
 __device__ __forceinline__ void store_zero_rows(const DecodeArgs& a, int G, int s, int kvh,
                                                 int nthreads) {
   T* out = static_cast<T*>(a.out);
-  for (int idx = threadIdx.x; idx < G * D; idx += nthreads) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    out[(static_cast<size_t>(s) * a.num_q_heads + kvh * G + h) * D + d] = Elem<T>::from_f(0.f);
+  for (int idx = threadIdx.x; idx < G * a.q_len * D; idx += nthreads) {
+    const int c = idx / D;
+    const int d = idx - c * D;
+    out[query_row(a, s, kvh, G, c) * D + d] = Elem<T>::from_f(0.f);
   }
 }
 

@@ -347,6 +347,7 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
   a.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_off) : nullptr;
   a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
   a.status = status;
+  a.q_len = 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -359,6 +360,89 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
     e = pa::launch_decode_tc(a, pool->dtype, kmap, vmap, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PA_OK;
+}
+
+size_t pa_verify_workspace_size(int num_seqs, int q_len, int num_q_heads, int max_context_len, int partition_size,
+                                const pa_pool_desc* pool) {
+  t_err.clear();
+  const int mb = (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  if (check_decode_shape(num_seqs, num_q_heads, mb, max_context_len, partition_size, pool) != PA_OK) return 0;
+  if (q_len < 1) {
+    fail(PA_ERR_INVALID, "q_len must be >= 1");
+    return 0;
+  }
+  const int p = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int ms = max_splits_for(max_context_len, p / PA_BLOCK_SIZE);
+  return ws_layout(num_seqs * q_len, num_q_heads, ms, pool->head_dim).total;
+}
+
+int pa_verify_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale, int num_seqs,
+                        int q_len, int num_q_heads, int max_blocks_per_seq, int max_context_len,
+                        int partition_size, const pa_pool_desc* pool, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  t_err.clear();
+  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
+  if (pool->dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "verify needs bf16 or fp16 pools");
+  if (q_len < 1) return fail(PA_ERR_INVALID, "q_len must be >= 1");
+  if ((num_q_heads / pool->num_kv_heads) * q_len > 32)
+    return fail(PA_ERR_UNSUPPORTED, "query group x q_len = %d > 32", (num_q_heads / pool->num_kv_heads) * q_len);
+  if (static_cast<long long>(num_seqs) * q_len > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many rows");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_pool || !v_pool || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(PA_ERR_INVALID, "out, q and the pools must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "block_tables and context_lens must be 4-byte aligned");
+
+  const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int part_blocks = part / PA_BLOCK_SIZE;
+  const int max_splits = max_splits_for(max_context_len, part_blocks);
+  const WsLayout ws = ws_layout(num_seqs * q_len, num_q_heads, max_splits, pool->head_dim);
+  if (ws.total > 0 && static_cast<long long>(num_seqs) * pool->num_kv_heads > kMaxCounters)
+    return fail(PA_ERR_UNSUPPORTED, "split-K over more than %d (sequence, KV head) pairs in one call",
+                kMaxCounters);
+  if (ws.total > 0) {
+    if (!workspace) return fail(PA_ERR_INVALID, "workspace of %zu bytes required, got NULL", ws.total);
+    if (workspace_bytes < ws.total)
+      return fail(PA_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, ws.total);
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+  }
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+
+  pa::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.head_dim = pool->head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.num_blocks = pool->num_blocks;
+  a.part_blocks = part_blocks;
+  a.max_splits = max_splits;
+  a.ws_count = ws.total ? static_cast<int*>(workspace) : nullptr;
+  a.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_off) : nullptr;
+  a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
+  a.status = status;
+  a.q_len = q_len;
+  CUtensorMap kmap, vmap;
+  if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
+  if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
+  cudaError_t e = pa::launch_decode_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return PA_OK;
 }
 
@@ -493,6 +577,7 @@ int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, cons
   a.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_off) : nullptr;
   a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
   a.status = status;
+  a.q_len = 1;
   CUtensorMap kmap, vmap;
   if ((rc = pool_map(&kmap, k_codes, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_codes, pool)) != PA_OK) return rc;

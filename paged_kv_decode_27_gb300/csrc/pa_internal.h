@@ -33,6 +33,7 @@ struct DecodeArgs {
   int* status;             // device status word (PA_DEV_* bits)
   const float* k_scales;   // INT8 cache only: [N_blk][H_kv][16] row scales
   const float* v_scales;
+  int q_len;               // query positions per sequence: 1 for decode, K+1 to verify K drafts
 };
 
 struct PrefillArgs {

@@ -165,6 +165,18 @@ class Workload:
                           context_lens=ctx, q_prefill=q_pre, cu_q_lens=cu,
                           prefill_context_lens=pre_ctx)
 
+    def verify_queries(self, t: int, q_len: int) -> torch.Tensor:
+        """Queries of a speculative-decoding verification pass at step t:
+        [S_dec][q_len][H_q][D], the last q_len cached positions of every
+        sequence (seeded separately from the step's other draws)."""
+        g = torch.Generator().manual_seed(((1000 + self.config_id) * 100 + t) * 16 + q_len)
+        return self._draw((self.num_decode_seqs, q_len, self.num_q_heads, self.head_dim), g)
+
+    def verify_bytes(self, t: int, q_len: int) -> int:
+        """decode_bytes with q_len query rows (q and out) per sequence."""
+        extra = 2 * (q_len - 1) * self.num_decode_seqs * self.num_q_heads * self.head_dim * self.elem_bytes
+        return self.decode_bytes(t) + extra
+
     def _draw(self, shape, g) -> torch.Tensor:
         x = torch.randn(shape, generator=g, dtype=torch.float32)
         if self.factor != 1.0:
@@ -371,7 +383,19 @@ WORKLOADS = {
     "mixed_mistral7b": mixed_mistral7b,
     "llama32_1b_decode_int8": lambda: llama32_1b_decode(kv="int8"),
     "llama3_8b_decode_int8": lambda: llama3_8b_decode(kv="int8"),
+    "llama3_8b_verify": lambda: llama3_8b_verify(),
 }
+
+
+def llama3_8b_verify(steps: int = 32, q_len: int = 5) -> Workload:
+    """The batch-64 Llama-3-8B-shaped decode batch in a speculative-decoding
+    verification pass: each sequence's last q_len = K + 1 = 5 positions (K = 4
+    drafted tokens) are queries, causal over the cache."""
+    wl = llama3_8b_decode(steps=steps)
+    wl.name = "llama3_8b_verify"
+    wl.description = "Llama-3-8B-shaped verification of K=4 drafts (q_len 5), bf16, batch 64"
+    wl.extra["verify_q_len"] = q_len
+    return wl
 
 
 def small_random(seed: int, num_seqs: int, max_ctx: int, hq: int, hkv: int, d: int,

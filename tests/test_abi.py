@@ -175,3 +175,20 @@ def test_int8_without_gpu_is_a_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _decode8(lib, _desc(dt=B.PA_I8)) == B.PA_ERR_CUDA
+
+
+def test_verify_validates_on_the_host(lib):
+    f = ctypes.c_void_p(FAKE)
+    call = lambda desc=_desc(), ql=5, hq=32, part=512: lib.pa_verify_attention(
+        f, f, f, f, f, f, 0.1, 4, ql, hq, 8, 100, part, ctypes.byref(desc), None, 0, None)
+    assert call(ql=0) == B.PA_ERR_INVALID
+    assert call(desc=_desc(dt=B.PA_F32)) == B.PA_ERR_UNSUPPORTED
+    assert call(desc=_desc(dt=B.PA_I8)) == B.PA_ERR_INVALID
+    assert call(hq=64, ql=5) == B.PA_ERR_UNSUPPORTED        # G 8 x 5 = 40 columns
+    # the verify workspace holds q_len rows per sequence; q_len 1 is the decode workspace
+    d = _desc()
+    assert lib.pa_verify_workspace_size(64, 1, 32, 8224, 0, ctypes.byref(d)) == \
+        lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(d))
+    rows = 64 * 5 * 32 * 9
+    assert lib.pa_verify_workspace_size(64, 5, 32, 8224, 0, ctypes.byref(d)) == \
+        ((256 * 1024 + rows * 128 * 4 + 255) // 256) * 256 + rows * 4

@@ -383,6 +383,22 @@ def test_prefill_row_equals_decode_at_that_position():
         assert np.array_equal(pre[i], dec[0])
 
 
+def test_prefill_query_before_the_context_is_zero():
+    """q_len larger than the context: the leading queries sit at negative
+    positions, see no key and give zero rows (the zero-context reading); the
+    others are ordinary causal rows."""
+    wl = W.small_random(19, num_seqs=1, max_ctx=1, hq=4, hkv=2, d=8, dtype=torch.float32, ctx=[3])
+    q = np.random.default_rng(3).standard_normal((5, 4, 8))
+    out = oracle.prefill_ref(q, to_np(wl.k_pool), to_np(wl.v_pool), wl.block_tables.numpy(),
+                             np.array([0, 5]), np.array([3]), 0.5)
+    assert not out[:2].any()
+    k = oracle.gather_contiguous(to_np(wl.k_pool), wl.block_tables[0].numpy(), 3)
+    v = oracle.gather_contiguous(to_np(wl.v_pool), wl.block_tables[0].numpy(), 3)
+    for i in range(2, 5):
+        ref = sdpa_rows(q[i:i + 1], k[:i - 1], v[:i - 1], 0.5)
+        assert np.max(np.abs(out[i] - ref[0])) < 1e-12
+
+
 def test_prefill_brute_force_tiny():
     wl, q, cu, ctx = _prefill_case(16, [3, 5], [2, 0], hq=2, hkv=1, d=3)
     kp, vp, bt = to_np(wl.k_pool), to_np(wl.v_pool), wl.block_tables.numpy()
