@@ -3,7 +3,7 @@
 Test infrastructure: only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may use it.  The CUDA path never imports it.
 Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle.py``
-and ``tests/test_oracle_int8.py``.
+``tests/test_oracle_int8.py`` and ``tests/test_oracle_rope.py``.
 """
 from .paged_attention import (  # noqa: F401
     BLOCK_SIZE,
@@ -23,3 +23,4 @@ from .kv_int8 import (  # noqa: F401,E402
     gather_dequantized,
     quantize_rows_int8,
 )
+from .rope import append_rope_ref, rope_cache_ref, rope_inv_freq, rope_rotate_ref  # noqa: F401,E402
