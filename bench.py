@@ -51,7 +51,7 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD,
                    help="llama3_8b_decode (the headline line) or one of tiny_fp32, llama32_1b_decode, "
                         "prefix_shared_8k, mixed_mistral7b, llama32_1b_decode_int8, llama3_8b_decode_int8, "
-                        "llama3_8b_verify (per-call figures for that workload)")
+                        "llama3_8b_verify, llama3_8b_decode_rope (per-call figures for that workload)")
     p.add_argument("--quick", action="store_true",
                    help="no CPU baseline, no 1 s pre-warm, no end-to-end pass (for profiler runs)")
     return p.parse_args()
@@ -464,6 +464,13 @@ def run_other(args):
         out = torch.empty((S, vq, hq, dh), dtype=wl.dtype, device=dev)
         ws = torch.zeros(max(1, pa.pa_verify_workspace_size(S, vq, hq, max_ctx, kp, args.partition)),
                          dtype=torch.uint8, device=dev)
+    theta = wl.extra.get("rope_theta")
+    if theta:   # RoPE: K rotated on the append, q rotated at position context - 1
+        cos_sin = torch.empty((max_ctx + 1, dh // 2, 2), dtype=torch.float32, device=dev)
+        pa.pa_rope_cache(cos_sin, theta)
+        for d in d_in:
+            d["pos"] = (d["ctx"] - 1).to(torch.int32)
+            d["q0"] = d["q"].clone()
     flush = torch.ones(256 << 20, dtype=torch.float16, device=dev)   # 512 MB, read to evict L2
     stream = torch.cuda.current_stream()
     rec = {"append": [], "prefill": [], "decode": []}
@@ -473,9 +480,14 @@ def run_other(args):
         if timed:
             flush.sum()   # reads 512 MB: evicts L2 without leaving dirty lines behind
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        if theta:
+            d["q"].copy_(d["q0"])   # the queries arrive unrotated every step
         evs[0].record(stream)
         if wl.kv_int8:
             pa.pa_append_kv_int8(kp, vp, ks, vs, d["slots"], d["kn"], d["vn"], stream=stream)
+        elif theta:
+            pa.pa_append_kv_rope(kp, vp, d["slots"], d["pos"], d["kn"], d["vn"], cos_sin, stream=stream)
+            pa.pa_apply_rope(d["q"], d["pos"], cos_sin, stream=stream)
         else:
             pa.pa_append_kv(kp, vp, d["slots"], d["kn"], d["vn"], stream=stream)
         evs[1].record(stream)
@@ -520,6 +532,9 @@ def run_other(args):
             "decode_frac_of_hbm_peak": dec_b / (med["decode"] * 1e-6) / 1e9 / peak, "hbm_peak": peak,
             "hbm_peak_kind": kind, "decode_bytes": dec_b,
             "decode_tokens_per_s": S / ((med["append"] + med["decode"] + med["prefill"]) * 1e-6)}
+    if theta:
+        line["rope_theta"] = theta
+        line["append_note"] = "append_us covers the RoPE append of K and the in-place rotation of q"
     if wl.prompt_lens:
         fl = wl.prefill_flops()
         line.update(prefill_us=med["prefill"], prefill_tflops=fl / (med["prefill"] * 1e-6) / 1e12,

@@ -68,7 +68,8 @@ enum {
   PA_DEV_BAD_SLOT = 1,        /* append: slot >= num_blocks*16 (row skipped)          */
   PA_DEV_BAD_BLOCK_ID = 2,    /* a block-table entry outside [0, num_blocks) (skipped) */
   PA_DEV_BAD_CONTEXT = 4,     /* context_len < 0 or > max_blocks_per_seq*16 (clamped) */
-  PA_DEV_WAIT_TIMEOUT = 8     /* a bounded wait on a copy barrier gave up              */
+  PA_DEV_WAIT_TIMEOUT = 8,    /* a bounded wait on a copy barrier gave up              */
+  PA_DEV_BAD_POSITION = 16    /* RoPE: position outside [0, max_positions) (row skipped) */
 };
 
 /* Geometry of the KV pool, shared by every call. */
@@ -285,6 +286,42 @@ PA_API int pa_decode_attention_int8(void* out, const void* q, const void* k_code
                                     int num_q_heads, int max_blocks_per_seq, int max_context_len,
                                     int partition_size, int act_dtype, const pa_pool_desc* pool,
                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Rotary position embedding fused into the append.  The pages name RoPE as a
+ * step to fuse with attention ("Mini inference engine", Story / portfolio:
+ * fuse qkv_proj + RoPE + attention) without defining it; this is the
+ * half-split rotary embedding of the Llama family: for position p, entries j
+ * and j + D/2 of a row (j < D/2) turn by the angle p * theta^(-2j/D):
+ *     x'[j] = x[j] cos - x[j + D/2] sin,   x'[j + D/2] = x[j + D/2] cos + x[j] sin.
+ *
+ * pa_rope_cache -- fill cos_sin, float32 [max_positions][head_dim/2][2] =
+ * (cos, sin) of p * theta^(-2j/head_dim), angles and trigonometry in float64,
+ * stored rounded to float32.  Build it once per model; the calls below read
+ * it.  Errors: PA_ERR_INVALID for a null or misaligned (8-byte) table,
+ * max_positions < 0 or theta <= 0; PA_ERR_UNSUPPORTED for head_dim not 64/128.
+ */
+PA_API int pa_rope_cache(float* cos_sin, int max_positions, int head_dim, double theta, void* stream);
+
+/*
+ * pa_append_kv_rope -- pa_append_kv with every K row rotated at its token's
+ * position (positions: int32 [num_tokens]) on the way into the pool: fp32
+ * arithmetic on the table entries, one rounding to the pool dtype.  V rows are
+ * copied bit for bit.  A position outside [0, max_positions) skips the token's
+ * K rows and sets PA_DEV_BAD_POSITION.  Errors as pa_append_kv, plus
+ * PA_ERR_INVALID for a null positions or cos_sin pointer.
+ */
+PA_API int pa_append_kv_rope(void* k_pool, void* v_pool, const int64_t* slot_mapping, const int32_t* positions,
+                             const void* k_new, const void* v_new, int num_tokens, const float* cos_sin,
+                             int max_positions, const pa_pool_desc* pool, void* stream);
+
+/*
+ * pa_apply_rope -- rotate rows x [num_tokens][num_heads][head_dim] (dtype
+ * PA_F32/PA_BF16/PA_F16) in place at their token's position: the queries of a
+ * step, before pa_decode_attention / pa_verify_attention.
+ */
+PA_API int pa_apply_rope(void* x, const int32_t* positions, int num_tokens, int num_heads, int head_dim,
+                         int dtype, const float* cos_sin, int max_positions, void* stream);
 
 /* Bytes of the per-device array behind pa_decode_attention_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)

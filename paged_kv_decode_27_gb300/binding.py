@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libp
 PA_F32, PA_BF16, PA_F16, PA_I8 = 0, 1, 2, 3
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = 0, -1, -2, -3, -4
 PA_DEV_BAD_SLOT, PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_CONTEXT, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
+PA_DEV_BAD_POSITION = 16
 BLOCK_SIZE = 16
 
 _DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16, torch.int8: PA_I8}
@@ -72,6 +73,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_verify_attention.restype = i32
     L.pa_verify_attention.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32, pdesc, vp, sz,
                                       vp]
+    L.pa_rope_cache.restype = i32
+    L.pa_rope_cache.argtypes = [vp, i32, i32, ctypes.c_double, vp]
+    L.pa_append_kv_rope.restype = i32
+    L.pa_append_kv_rope.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, pdesc, vp]
+    L.pa_apply_rope.restype = i32
+    L.pa_apply_rope.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
     L.pa_append_kv_int8.restype = i32
     L.pa_append_kv_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, pdesc, vp]
     L.pa_decode_attention_int8.restype = i32
@@ -362,3 +369,53 @@ def pa_decode_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.
                                       int(block_tables.shape[1]), int(max_context_len), int(partition_size),
                                       _act(q), ctypes.byref(desc), _ptr(workspace), int(ws_bytes),
                                       _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# rotary position embedding (half-split, Llama form)
+# ---------------------------------------------------------------------------
+
+def pa_rope_cache(cos_sin: torch.Tensor, theta: float, stream=None) -> None:
+    """Fill cos_sin, float32 CUDA [max_positions][D/2][2], with (cos, sin) of
+    p * theta^(-2j/D)."""
+    _cuda_contig("cos_sin", cos_sin)
+    _need(cos_sin.dtype == torch.float32 and cos_sin.dim() == 3 and cos_sin.shape[2] == 2,
+          "cos_sin must be float32 [max_positions][D/2][2]")
+    L = load_library()
+    _check(L.pa_rope_cache(_ptr(cos_sin), int(cos_sin.shape[0]), int(2 * cos_sin.shape[1]), float(theta),
+                           _stream(stream)))
+
+
+def pa_append_kv_rope(k_pool: torch.Tensor, v_pool: torch.Tensor, slot_mapping: torch.Tensor,
+                      positions: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cos_sin: torch.Tensor,
+                      stream=None) -> None:
+    """pa_append_kv with K rotated at positions (int32 [T]) on the way in."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("slot_mapping", slot_mapping), ("positions", positions), ("k_new", k_new), ("v_new", v_new),
+                 ("cos_sin", cos_sin)):
+        _cuda_contig(n, t)
+    T = slot_mapping.shape[0]
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.dim() == 1, "slot_mapping must be int64 [T]")
+    _need(positions.dtype == torch.int32 and tuple(positions.shape) == (T,), "positions must be int32 [T]")
+    shape = (T, k_pool.shape[1], k_pool.shape[3])
+    _need(tuple(k_new.shape) == shape and tuple(v_new.shape) == shape, f"k_new/v_new must be {shape}")
+    _need(k_new.dtype == k_pool.dtype and v_new.dtype == k_pool.dtype, "k_new/v_new dtype must match the pool")
+    _need(cos_sin.dtype == torch.float32 and cos_sin.dim() == 3 and cos_sin.shape[1] * 2 == k_pool.shape[3],
+          "cos_sin must be float32 [max_positions][D/2][2]")
+    L = load_library()
+    _check(L.pa_append_kv_rope(_ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping), _ptr(positions), _ptr(k_new),
+                               _ptr(v_new), int(T), _ptr(cos_sin), int(cos_sin.shape[0]), ctypes.byref(desc),
+                               _stream(stream)))
+
+
+def pa_apply_rope(x: torch.Tensor, positions: torch.Tensor, cos_sin: torch.Tensor, stream=None) -> None:
+    """Rotate x [T][H][D] in place at positions (int32 [T])."""
+    for n, t in (("x", x), ("positions", positions), ("cos_sin", cos_sin)):
+        _cuda_contig(n, t)
+    _need(x.dim() == 3 and x.dtype in _DTYPES and x.dtype != torch.int8, "x must be [T][H][D] fp32/bf16/fp16")
+    _need(positions.dtype == torch.int32 and tuple(positions.shape) == (x.shape[0],), "positions must be int32 [T]")
+    _need(cos_sin.dtype == torch.float32 and cos_sin.dim() == 3 and cos_sin.shape[1] * 2 == x.shape[2],
+          "cos_sin must be float32 [max_positions][D/2][2]")
+    L = load_library()
+    _check(L.pa_apply_rope(_ptr(x), _ptr(positions), int(x.shape[0]), int(x.shape[1]), int(x.shape[2]),
+                           _DTYPES[x.dtype], _ptr(cos_sin), int(cos_sin.shape[0]), _stream(stream)))

@@ -586,6 +586,65 @@ int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, cons
   return PA_OK;
 }
 
+int pa_rope_cache(float* cos_sin, int max_positions, int head_dim, double theta, void* stream) {
+  t_err.clear();
+  if (head_dim != 64 && head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d not supported", head_dim);
+  if (max_positions < 0) return fail(PA_ERR_INVALID, "max_positions must be >= 0");
+  if (!(theta > 0.0) || !std::isfinite(theta)) return fail(PA_ERR_INVALID, "theta must be positive and finite");
+  if (max_positions == 0) return PA_OK;
+  if (!cos_sin || (reinterpret_cast<uintptr_t>(cos_sin) & 7u))
+    return fail(PA_ERR_INVALID, "cos_sin must be a non-null 8-byte aligned pointer");
+  cudaError_t e = pa::launch_rope_cache(cos_sin, max_positions, head_dim, theta, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope cache launch");
+  return PA_OK;
+}
+
+int pa_append_kv_rope(void* k_pool, void* v_pool, const int64_t* slot_mapping, const int32_t* positions,
+                      const void* k_new, const void* v_new, int num_tokens, const float* cos_sin, int max_positions,
+                      const pa_pool_desc* pool, void* stream) {
+  t_err.clear();
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens must be >= 0");
+  if (max_positions < 0) return fail(PA_ERR_INVALID, "max_positions must be >= 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!k_pool || !v_pool || !slot_mapping || !positions || !k_new || !v_new || !cos_sin)
+    return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(PA_ERR_INVALID, "pools and k_new/v_new must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(positions) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cos_sin) & 7u))
+    return fail(PA_ERR_INVALID, "slot_mapping (8), positions (4) or cos_sin (8 bytes) misaligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  cudaError_t e = pa::launch_append_rope(k_pool, v_pool, slot_mapping, positions, k_new, v_new, cos_sin,
+                                         max_positions, num_tokens, pool->num_kv_heads, pool->head_dim, pool->dtype,
+                                         pool->num_blocks, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append_kv_rope launch");
+  return PA_OK;
+}
+
+int pa_apply_rope(void* x, const int32_t* positions, int num_tokens, int num_heads, int head_dim, int dtype,
+                  const float* cos_sin, int max_positions, void* stream) {
+  t_err.clear();
+  if (head_dim != 64 && head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d not supported", head_dim);
+  if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_F16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+  if (num_tokens < 0 || num_heads < 1 || max_positions < 0)
+    return fail(PA_ERR_INVALID, "num_tokens >= 0, num_heads >= 1 and max_positions >= 0 required");
+  if (num_tokens == 0) return PA_OK;
+  if (!x || !positions || !cos_sin) return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(positions) & 3u) || (reinterpret_cast<uintptr_t>(cos_sin) & 7u))
+    return fail(PA_ERR_INVALID, "x (16), positions (4) or cos_sin (8 bytes) misaligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  cudaError_t e = pa::launch_apply_rope(x, positions, cos_sin, max_positions, num_tokens, num_heads, head_dim, dtype,
+                                        status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "apply_rope launch");
+  return PA_OK;
+}
+
 int pa_device_status(int* status, void* stream) {
   t_err.clear();
   if (!status) return fail(PA_ERR_INVALID, "status pointer is NULL");

@@ -77,6 +77,16 @@ cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scales, floa
 cudaError_t launch_decode_q8(const DecodeArgs& a, int act_dtype, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream);
 
+// Rotary position embedding: the (cos, sin) table, K rotated on append, rows in place.
+cudaError_t launch_rope_cache(float* cos_sin, int max_positions, int head_dim, double theta, cudaStream_t stream);
+cudaError_t launch_append_rope(void* k_pool, void* v_pool, const int64_t* slot_mapping, const int32_t* positions,
+                               const void* k_new, const void* v_new, const float* cos_sin, int max_positions,
+                               int num_tokens, int num_kv_heads, int head_dim, int dtype, int num_blocks,
+                               int* status, cudaStream_t stream);
+cudaError_t launch_apply_rope(void* x, const int32_t* positions, const float* cos_sin, int max_positions,
+                              int num_tokens, int num_heads, int head_dim, int dtype, int* status,
+                              cudaStream_t stream);
+
 // Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).
 cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, cudaStream_t stream);

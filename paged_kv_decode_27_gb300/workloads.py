@@ -384,7 +384,19 @@ WORKLOADS = {
     "llama32_1b_decode_int8": lambda: llama32_1b_decode(kv="int8"),
     "llama3_8b_decode_int8": lambda: llama3_8b_decode(kv="int8"),
     "llama3_8b_verify": lambda: llama3_8b_verify(),
+    "llama3_8b_decode_rope": lambda: llama3_8b_decode_rope(),
 }
+
+
+def llama3_8b_decode_rope(steps: int = 32) -> Workload:
+    """The batch-64 Llama-3-8B-shaped decode with rotary position embedding
+    (theta 500000, Llama 3's base) applied to K on the append and to q before
+    attention."""
+    wl = llama3_8b_decode(steps=steps)
+    wl.name = "llama3_8b_decode_rope"
+    wl.description = "Llama-3-8B-shaped decode with RoPE (theta 5e5) fused into the append, bf16, batch 64"
+    wl.extra["rope_theta"] = 500000.0
+    return wl
 
 
 def llama3_8b_verify(steps: int = 32, q_len: int = 5) -> Workload:

@@ -192,3 +192,19 @@ def test_verify_validates_on_the_host(lib):
     rows = 64 * 5 * 32 * 9
     assert lib.pa_verify_workspace_size(64, 5, 32, 8224, 0, ctypes.byref(d)) == \
         ((256 * 1024 + rows * 128 * 4 + 255) // 256) * 256 + rows * 4
+
+
+def test_rope_entry_points_validate_on_the_host(lib):
+    f = ctypes.c_void_p(FAKE)
+    assert lib.pa_rope_cache(f, 10, 96, ctypes.c_double(1e4), None) == B.PA_ERR_UNSUPPORTED
+    assert lib.pa_rope_cache(f, 10, 128, ctypes.c_double(0.0), None) == B.PA_ERR_INVALID
+    assert lib.pa_rope_cache(ctypes.c_void_p(FAKE + 4), 10, 128, ctypes.c_double(1e4), None) == B.PA_ERR_INVALID
+    assert lib.pa_rope_cache(f, 0, 128, ctypes.c_double(1e4), None) == B.PA_OK
+    d = _desc()
+    app = lambda pos=f, T=4, desc=d: lib.pa_append_kv_rope(f, f, f, pos, f, f, T, f, 100, ctypes.byref(desc), None)
+    assert app(pos=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
+    assert app(pos=ctypes.c_void_p(FAKE + 2)) == B.PA_ERR_INVALID
+    assert app(desc=_desc(dt=B.PA_I8)) == B.PA_ERR_INVALID
+    assert app(T=0) == B.PA_OK
+    assert lib.pa_apply_rope(f, f, 4, 8, 128, B.PA_I8, f, 100, None) == B.PA_ERR_UNSUPPORTED
+    assert lib.pa_apply_rope(ctypes.c_void_p(FAKE + 8), f, 4, 8, 128, B.PA_BF16, f, 100, None) == B.PA_ERR_INVALID
