@@ -51,7 +51,8 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD,
                    help="llama3_8b_decode (the headline line) or one of tiny_fp32, llama32_1b_decode, "
                         "prefix_shared_8k, mixed_mistral7b, llama32_1b_decode_int8, llama3_8b_decode_int8, "
-                        "llama3_8b_verify, llama3_8b_decode_rope (per-call figures for that workload)")
+                        "llama3_8b_verify, llama3_8b_decode_rope (per-call figures for that workload), or "
+                        "llama3_8b_prefix_serving (decode steps driven by the block manager)")
     p.add_argument("--quick", action="store_true",
                    help="no CPU baseline, no 1 s pre-warm, no end-to-end pass (for profiler runs)")
     return p.parse_args()
@@ -543,6 +544,90 @@ def run_other(args):
     print(json.dumps(line), flush=True)
 
 
+def run_serving(args):
+    """Decode steps driven by the block manager with a prefix cache: 64
+    sequences whose prompts share a 208-token system prompt (13 blocks) and
+    whose contexts are log-uniform in [512, 8192] (the Llama-3-8B-shaped
+    decode batch).  Every step appends one token per sequence through the
+    manager (host), uploads slots and block tables, appends K/V and decodes.
+    Reports the manager's host time per step beside the GPU time."""
+    import math
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_decode_27_gb300 import binding as pa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    S, hq, hkv, d, sys_len = 64, 32, 8, 128, 208
+    g = torch.Generator().manual_seed(2024)
+    u = torch.rand((S,), generator=g, dtype=torch.float64)
+    ctx0 = torch.floor(torch.exp(math.log(512) + u * (math.log(8192) - math.log(512)))).to(torch.int64)
+    steps_total = args.warmup + args.steps
+    mb = (int(ctx0.max()) + steps_total + 15) // 16
+    nb = int(1.1 * (sum((int(c) + steps_total + 15) // 16 for c in ctx0)))
+    bm = pa.pa_bm_create(nb, mb, S)
+    system = torch.randint(0, 32000, (sys_len,), generator=g).tolist()
+    t0 = time.perf_counter()
+    cached = 0
+    for s in range(S):
+        prompt = system + torch.randint(0, 32000, (int(ctx0[s]) - sys_len,), generator=g).tolist()
+        cached += pa.pa_bm_add_sequence(bm, s, prompt)[0]
+    add_s = time.perf_counter() - t0
+    kp = torch.randn((nb, hkv, 16, d), generator=g).to(torch.bfloat16).to(dev)
+    vp = torch.randn((nb, hkv, 16, d), generator=g).to(torch.bfloat16).to(dev)
+    q = torch.randn((S, hq, d), generator=g).to(torch.bfloat16).to(dev)
+    kn = torch.randn((S, hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    vn = torch.randn((S, hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    out = torch.empty_like(q)
+    max_ctx = mb * 16
+    ws = torch.zeros(max(1, pa.pa_decode_workspace_size(S, hq, max_ctx, kp)), dtype=torch.uint8, device=dev)
+    slot_h = torch.empty((S,), dtype=torch.int64).pin_memory()
+    tab_h = torch.empty((S, mb), dtype=torch.int32).pin_memory()
+    ctx_h = torch.empty((S,), dtype=torch.int32).pin_memory()
+    slot_d = torch.empty((S,), dtype=torch.int64, device=dev)
+    tab_d = torch.empty((S, mb), dtype=torch.int32, device=dev)
+    ctx_d = torch.empty((S,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    host_us, step_us, gpu_us = [], [], []
+    ids_np = np.arange(S, dtype=np.int32)
+    for it in range(steps_total):
+        tw0 = time.perf_counter()
+        toks = np.full(S, it % 32000, dtype=np.int32)
+        _, copies = pa.pa_bm_append_step(bm, ids_np, toks, slots_out=slot_h)
+        pa.pa_bm_block_tables_into(bm, ids_np, tab_h, ctx_h)
+        th = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        slot_d.copy_(slot_h, non_blocking=True)
+        tab_d.copy_(tab_h, non_blocking=True)
+        ctx_d.copy_(ctx_h, non_blocking=True)
+        e0.record(stream)
+        pa.pa_append_kv(kp, vp, slot_d, kn, vn, stream=stream)
+        pa.pa_decode_attention(out, q, kp, vp, tab_d, ctx_d, 1.0 / math.sqrt(d), max_context_len=max_ctx,
+                               workspace=ws, stream=stream)
+        e1.record(stream)
+        stream.synchronize()
+        te = time.perf_counter()
+        if it >= args.warmup:
+            host_us.append((th - tw0) * 1e6)
+            step_us.append((te - tw0) * 1e6)
+            gpu_us.append(e0.elapsed_time(e1) * 1e3)
+    st = pa.pa_bm_get_stats(bm)
+    pa.pa_bm_destroy(bm)
+    line = {"workload": "llama3_8b_prefix_serving",
+            "description": "64 sequences sharing a 208-token system prompt, contexts log-uniform in [512, 8192], "
+                           "one token per sequence per step through the block manager",
+            "steps": args.steps, "warmup": args.warmup,
+            "prompt_tokens_from_prefix_cache": cached, "add_sequences_ms": add_s * 1e3,
+            "manager_host_us_per_step": statistics.median(host_us),
+            "manager_host_us_per_token": statistics.median(host_us) / S,
+            "gpu_us_per_step": statistics.median(gpu_us), "wall_us_per_step": statistics.median(step_us),
+            "manager_stats": st, "device_status": pa.pa_device_status()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -554,7 +639,10 @@ def main():
     if args.workload != WORKLOAD:
         if world > 1:
             raise SystemExit("--workload other than the headline runs on one GPU")
-        run_other(args)
+        if args.workload == "llama3_8b_prefix_serving":
+            run_serving(args)
+        else:
+            run_other(args)
         return
     if world > 1:
         import torch

@@ -60,7 +60,8 @@ enum {
   PA_ERR_INVALID = -1,     /* bad argument (null, misaligned, inconsistent sizes) */
   PA_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, dtype or group size  */
   PA_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed          */
-  PA_ERR_DEVICE = -4       /* pa_device_status found a flagged device-side problem */
+  PA_ERR_DEVICE = -4,      /* pa_device_status found a flagged device-side problem */
+  PA_ERR_NO_BLOCKS = -5    /* block manager: no free or evictable block left       */
 };
 
 /* bits of the device status word */
@@ -322,6 +323,87 @@ PA_API int pa_append_kv_rope(void* k_pool, void* v_pool, const int64_t* slot_map
  */
 PA_API int pa_apply_rope(void* x, const int32_t* positions, int num_tokens, int num_heads, int head_dim,
                          int dtype, const float* cos_sin, int max_positions, void* stream);
+
+/*
+ * Block manager with a prefix cache (host side).  The paged pool of 16-token
+ * blocks reached through per-sequence block tables ("LLM Inference Server",
+ * Optional Bonus Extensions: Paged KV-Cache Block Allocator; "LLM Inference
+ * Server From Scratch", How it works, 3 Block Manager), with the hash-keyed
+ * prefix cache of "LLM Inference Server", Stage 1 (a shared system prompt's KV
+ * stored once and reused; hit/miss tracking).  The manager only does the
+ * bookkeeping: it hands out slots (for pa_append_kv and friends), block tables
+ * (for the attention calls) and copy-on-write pairs (for pa_copy_blocks).
+ *
+ * Policies, deterministic: full blocks are keyed by FNV-1a 64 over the
+ * little-endian bytes of (parent block key, 16 token ids), content checked on
+ * a hit; a prompt reuses its cached full blocks from the start up to the first
+ * miss; new full blocks are cached at once; appending into a last block that
+ * another table holds copies it first; freeing releases blocks last to first,
+ * cached ones onto a least-recently-released list; allocation takes the
+ * lowest free id, else evicts the least recently released cached block.  A
+ * call that runs out of blocks returns PA_ERR_NO_BLOCKS and changes nothing.
+ * A manager is not thread-safe.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+typedef struct {
+  int64_t hit_blocks;     /* prompt blocks found in the prefix cache            */
+  int64_t miss_blocks;    /* full prompt blocks not found                       */
+  int64_t cow_copies;     /* copy-on-write pairs handed out                      */
+  int64_t evictions;      /* cached idle blocks reused for new data              */
+  int32_t free_blocks;    /* never used or released uncached                    */
+  int32_t cached_free_blocks; /* released, still cached, evictable             */
+  int32_t used_blocks;    /* held by at least one table                         */
+} pa_bm_stats;
+
+/* A manager for num_blocks blocks, tables of up to max_blocks_per_seq
+ * entries, sequence ids 0..max_seqs-1.  NULL on bad arguments. */
+PA_API pa_block_manager* pa_bm_create(int num_blocks, int max_blocks_per_seq, int max_seqs);
+PA_API void pa_bm_destroy(pa_block_manager* bm);
+
+/* Start sequence `seq` with prompt token ids [prompt_len].  slots (int64
+ * [prompt_len], host) receives the pool slot of every prompt position; the
+ * return value (>= 0) is the number of leading prompt tokens whose blocks came
+ * from the prefix cache (their K/V are already in the pool), else an error. */
+PA_API int pa_bm_add_sequence(pa_block_manager* bm, int seq, const int32_t* prompt, int prompt_len,
+                              int64_t* slots);
+
+/* Append n tokens to `seq`: slots (int64 [n], host) receives their pool
+ * slots.  When the sequence's last block is shared with another table it is
+ * copied first: the pair (source block, new block) goes to copies (int32,
+ * room for max_copies pairs; at most one pair per call) and *num_copies is
+ * set; the caller runs pa_copy_blocks before writing the new tokens. */
+PA_API int pa_bm_append(pa_block_manager* bm, int seq, const int32_t* tokens, int n, int64_t* slots,
+                        int32_t* copies, int max_copies, int* num_copies);
+
+/* One decode step: token tokens[i] appended to sequence seq_ids[i] for i < n
+ * (distinct sequences), in order, all or nothing.  slots: int64 [n];
+ * copy-on-write pairs (at most one per sequence) go to copies, in call
+ * order.  The same result as n single-token pa_bm_append calls. */
+PA_API int pa_bm_append_step(pa_block_manager* bm, const int32_t* seq_ids, const int32_t* tokens, int n,
+                             int64_t* slots, int32_t* copies, int max_copies, int* num_copies);
+
+/* `child` shares every block of `parent` (e.g. several samples of one prompt). */
+PA_API int pa_bm_fork(pa_block_manager* bm, int parent, int child);
+
+/* End `seq` and release its blocks. */
+PA_API int pa_bm_free_sequence(pa_block_manager* bm, int seq);
+
+/* Block tables (int32 [n][max_blocks], unused entries 0) and context lengths
+ * (int32 [n]) of the listed live sequences, in host memory. */
+PA_API int pa_bm_block_tables(const pa_block_manager* bm, const int32_t* seq_ids, int n, int32_t* tables,
+                              int max_blocks, int32_t* context_lens);
+
+PA_API int pa_bm_get_stats(const pa_block_manager* bm, pa_bm_stats* out);
+
+/*
+ * pa_copy_blocks -- copy whole pool blocks (every KV head, K and V) for
+ * copy-on-write: pairs (int32 [num_pairs][2], DEVICE) = (source, destination)
+ * block ids, destinations distinct and not sources.  Bit-exact.  Ids outside
+ * the pool are skipped and set PA_DEV_BAD_BLOCK_ID.  Float pools only.
+ */
+PA_API int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs,
+                          const pa_pool_desc* pool, void* stream);
 
 /* Bytes of the per-device array behind pa_decode_attention_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)

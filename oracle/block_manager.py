@@ -182,6 +182,32 @@ class BlockManagerRef:
                 s["tail"] = []
         return slots, copies
 
+    def append_step(self, seqs: List[int], tokens: List[int]):
+        """One token for each listed sequence (in order), all or nothing:
+        returns (slots, copy-on-write pairs in call order)."""
+        need, dec = 0, {}
+        for sq in seqs:
+            s = self.seqs[sq]
+            if (s["len"] + 1 + BLOCK - 1) // BLOCK > self.max_blocks:
+                raise ValueError("sequence longer than the block table")
+            if s["len"] % BLOCK == 0:
+                need += 1
+            else:
+                last = s["table"][-1]
+                if self.ref[last] - dec.get(last, 0) > 1:
+                    need += 1
+                    dec[last] = dec.get(last, 0) + 1
+        if len(set(seqs)) != len(seqs):
+            raise ValueError("a sequence listed twice")
+        if self._available() < need:
+            raise NoBlocks()
+        slots, copies = [], []
+        for sq, tok in zip(seqs, tokens):
+            sl, cp = self.append(sq, [tok])
+            slots += sl
+            copies += cp
+        return slots, copies
+
     def fork(self, parent: int, child: int):
         if child in self.seqs or not (0 <= child < self.max_seqs):
             raise ValueError("bad child id")

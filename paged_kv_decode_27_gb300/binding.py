@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libp
 
 PA_F32, PA_BF16, PA_F16, PA_I8 = 0, 1, 2, 3
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = 0, -1, -2, -3, -4
+PA_ERR_NO_BLOCKS = -5
 PA_DEV_BAD_SLOT, PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_CONTEXT, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 PA_DEV_BAD_POSITION = 16
 BLOCK_SIZE = 16
@@ -34,6 +35,12 @@ class PaError(RuntimeError):
 class pa_pool_desc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("block_size", ctypes.c_int), ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class pa_bm_stats(ctypes.Structure):
+    _fields_ = [("hit_blocks", ctypes.c_int64), ("miss_blocks", ctypes.c_int64), ("cow_copies", ctypes.c_int64),
+                ("evictions", ctypes.c_int64), ("free_blocks", ctypes.c_int32),
+                ("cached_free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32)]
 
 
 _lib = None
@@ -79,6 +86,26 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_append_kv_rope.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, pdesc, vp]
     L.pa_apply_rope.restype = i32
     L.pa_apply_rope.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, vp]
+    L.pa_bm_create.restype = vp
+    L.pa_bm_create.argtypes = [i32, i32, i32]
+    L.pa_bm_destroy.restype = None
+    L.pa_bm_destroy.argtypes = [vp]
+    L.pa_bm_add_sequence.restype = i32
+    L.pa_bm_add_sequence.argtypes = [vp, i32, vp, i32, vp]
+    L.pa_bm_append.restype = i32
+    L.pa_bm_append.argtypes = [vp, i32, vp, i32, vp, vp, i32, ctypes.POINTER(ctypes.c_int)]
+    L.pa_bm_append_step.restype = i32
+    L.pa_bm_append_step.argtypes = [vp, vp, vp, i32, vp, vp, i32, ctypes.POINTER(ctypes.c_int)]
+    L.pa_bm_fork.restype = i32
+    L.pa_bm_fork.argtypes = [vp, i32, i32]
+    L.pa_bm_free_sequence.restype = i32
+    L.pa_bm_free_sequence.argtypes = [vp, i32]
+    L.pa_bm_block_tables.restype = i32
+    L.pa_bm_block_tables.argtypes = [vp, vp, i32, vp, i32, vp]
+    L.pa_bm_get_stats.restype = i32
+    L.pa_bm_get_stats.argtypes = [vp, ctypes.POINTER(pa_bm_stats)]
+    L.pa_copy_blocks.restype = i32
+    L.pa_copy_blocks.argtypes = [vp, vp, vp, i32, pdesc, vp]
     L.pa_append_kv_int8.restype = i32
     L.pa_append_kv_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, pdesc, vp]
     L.pa_decode_attention_int8.restype = i32
@@ -419,3 +446,105 @@ def pa_apply_rope(x: torch.Tensor, positions: torch.Tensor, cos_sin: torch.Tenso
     L = load_library()
     _check(L.pa_apply_rope(_ptr(x), _ptr(positions), int(x.shape[0]), int(x.shape[1]), int(x.shape[2]),
                            _DTYPES[x.dtype], _ptr(cos_sin), int(cos_sin.shape[0]), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# block manager with a prefix cache (host side)
+# ---------------------------------------------------------------------------
+
+def _i32(xs) -> "np.ndarray":
+    import numpy as np
+    return np.ascontiguousarray(np.asarray(xs, dtype=np.int32))
+
+
+def pa_bm_create(num_blocks: int, max_blocks_per_seq: int, max_seqs: int) -> ctypes.c_void_p:
+    h = load_library().pa_bm_create(int(num_blocks), int(max_blocks_per_seq), int(max_seqs))
+    if not h:
+        raise PaError(PA_ERR_INVALID, pa_last_error())
+    return ctypes.c_void_p(h)
+
+
+def pa_bm_destroy(bm) -> None:
+    load_library().pa_bm_destroy(bm)
+
+
+def pa_bm_add_sequence(bm, seq: int, prompt):
+    """-> (number of prompt tokens found in the prefix cache, int64 slots of every prompt position)."""
+    import numpy as np
+    p = _i32(prompt)
+    slots = np.zeros(max(1, p.size), dtype=np.int64)
+    rc = load_library().pa_bm_add_sequence(bm, int(seq), p.ctypes.data, int(p.size), slots.ctypes.data)
+    if rc < 0:
+        raise PaError(rc, pa_last_error())
+    return rc, slots[:p.size]
+
+
+def pa_bm_append(bm, seq: int, tokens):
+    """-> (int64 slots of the new tokens, list of copy-on-write pairs (src, dst))."""
+    import numpy as np
+    t = _i32(tokens)
+    slots = np.zeros(max(1, t.size), dtype=np.int64)
+    copies = np.zeros(2, dtype=np.int32)
+    n = ctypes.c_int(0)
+    _check(load_library().pa_bm_append(bm, int(seq), t.ctypes.data, int(t.size), slots.ctypes.data,
+                                       copies.ctypes.data, 1, ctypes.byref(n)))
+    return slots[:t.size], [(int(copies[2 * i]), int(copies[2 * i + 1])) for i in range(n.value)]
+
+
+def pa_bm_append_step(bm, seq_ids, tokens, slots_out=None):
+    """One token per listed sequence.  -> (int64 slots, copy-on-write pairs).
+    ``slots_out`` (int64 array or pinned CPU tensor of len(seq_ids)) receives
+    the slots in place when given."""
+    import numpy as np
+    ids, toks = _i32(seq_ids), _i32(tokens)
+    _need(ids.size == toks.size, "one token per sequence")
+    if slots_out is None:
+        slots_out = np.zeros(max(1, ids.size), dtype=np.int64)
+    ptr = slots_out.data_ptr() if hasattr(slots_out, "data_ptr") else slots_out.ctypes.data
+    copies = np.zeros(2 * max(1, ids.size), dtype=np.int32)
+    n = ctypes.c_int(0)
+    _check(load_library().pa_bm_append_step(bm, ids.ctypes.data, toks.ctypes.data, int(ids.size), ptr,
+                                            copies.ctypes.data, max(1, ids.size), ctypes.byref(n)))
+    return slots_out, [(int(copies[2 * i]), int(copies[2 * i + 1])) for i in range(n.value)]
+
+
+def pa_bm_block_tables_into(bm, seq_ids, tables_out, ctx_out) -> None:
+    """pa_bm_block_tables writing into given int32 host buffers (e.g. pinned
+    tensors [n][max_blocks] and [n])."""
+    ids = _i32(seq_ids)
+    _check(load_library().pa_bm_block_tables(bm, ids.ctypes.data, int(ids.size), tables_out.data_ptr(),
+                                             int(tables_out.shape[1]), ctx_out.data_ptr()))
+
+
+def pa_bm_fork(bm, parent: int, child: int) -> None:
+    _check(load_library().pa_bm_fork(bm, int(parent), int(child)))
+
+
+def pa_bm_free_sequence(bm, seq: int) -> None:
+    _check(load_library().pa_bm_free_sequence(bm, int(seq)))
+
+
+def pa_bm_block_tables(bm, seq_ids, max_blocks: int):
+    """-> (int32 [n][max_blocks] tables, int32 [n] context lengths), host numpy."""
+    import numpy as np
+    ids = _i32(seq_ids)
+    tables = np.zeros((max(1, ids.size), max_blocks), dtype=np.int32)
+    ctx = np.zeros(max(1, ids.size), dtype=np.int32)
+    _check(load_library().pa_bm_block_tables(bm, ids.ctypes.data, int(ids.size), tables.ctypes.data,
+                                             int(max_blocks), ctx.ctypes.data))
+    return tables[:ids.size], ctx[:ids.size]
+
+
+def pa_bm_get_stats(bm) -> dict:
+    st = pa_bm_stats()
+    _check(load_library().pa_bm_get_stats(bm, ctypes.byref(st)))
+    return {name: int(getattr(st, name)) for name, _ in pa_bm_stats._fields_}
+
+
+def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, pairs: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks for copy-on-write; pairs: int32 CUDA [n][2] (src, dst)."""
+    desc = _pools(k_pool, v_pool)
+    _cuda_contig("pairs", pairs)
+    _need(pairs.dtype == torch.int32 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs must be int32 [n][2]")
+    _check(load_library().pa_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), int(pairs.shape[0]),
+                                         ctypes.byref(desc), _stream(stream)))

@@ -1,6 +1,7 @@
 """Build libpa.so (the C-ABI CUDA library) in-tree with nvcc for sm_103a.
 
-Each ``csrc/*.cu`` file is compiled in parallel to an object file, then the
+Each ``csrc/*.cu`` (device code) and ``csrc/*.cpp`` (host code) file is
+compiled in parallel to an object file, then the
 objects are linked into ``paged_kv_decode_27_gb300/lib/libpa.so`` with the CUDA
 runtime linked statically.  Nothing is rebuilt when the objects are newer than
 their sources and headers.
@@ -37,7 +38,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _headers():
@@ -71,7 +72,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
     jobs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         if force or ptxas_info or _stale(obj, [src, *hdrs]):
             jobs.append((src, obj))

@@ -645,6 +645,26 @@ int pa_apply_rope(void* x, const int32_t* positions, int num_tokens, int num_hea
   return PA_OK;
 }
 
+int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, const pa_pool_desc* pool,
+                   void* stream) {
+  t_err.clear();
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
+  if (num_pairs < 0) return fail(PA_ERR_INVALID, "num_pairs must be >= 0");
+  if (num_pairs == 0) return PA_OK;
+  if (!k_pool || !v_pool || !pairs) return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(pairs) & 7u))
+    return fail(PA_ERR_INVALID, "pools must be 16-byte and pairs 8-byte aligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  const int block_bytes = pool->num_kv_heads * PA_BLOCK_SIZE * pool->head_dim * elem_bytes(pool->dtype);
+  cudaError_t e = pa::launch_copy_blocks(k_pool, v_pool, pairs, num_pairs, block_bytes, pool->num_blocks, status,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PA_OK;
+}
+
 int pa_device_status(int* status, void* stream) {
   t_err.clear();
   if (!status) return fail(PA_ERR_INVALID, "status pointer is NULL");

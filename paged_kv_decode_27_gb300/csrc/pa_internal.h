@@ -87,6 +87,10 @@ cudaError_t launch_apply_rope(void* x, const int32_t* positions, const float* co
                               int num_tokens, int num_heads, int head_dim, int dtype, int* status,
                               cudaStream_t stream);
 
+// Copy-on-write: whole pool blocks (all heads, K and V), pairs (src, dst) on the device.
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, int block_bytes,
+                               int num_blocks, int* status, cudaStream_t stream);
+
 // Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).
 cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, cudaStream_t stream);

@@ -251,3 +251,23 @@ def test_eviction_order_scenario(w=None):
     w.add(2, list(range(200, 232)))
     w.add(3, list(range(300, 316)))
     assert w.m.table(3) == [3]
+
+
+def test_append_step_equals_single_appends_and_is_all_or_nothing():
+    w1, w2 = World(nb=12, max_blocks=8, max_seqs=6), World(nb=12, max_blocks=8, max_seqs=6)
+    for w in (w1, w2):
+        w.add(0, list(range(20)))
+        w.fork(0, 1)
+        w.fork(0, 2)                               # three tables share the partial block
+    slots, copies = w1.m.append_step([1, 2, 0], [7, 8, 9])
+    singles = [w2.m.append(s, [t]) for s, t in ((1, 7), (2, 8), (0, 9))]
+    assert slots == [x for sl, _ in singles for x in sl] and copies == [c for _, cp in singles for c in cp]
+    assert len(copies) == 2                        # the last of the three keeps the block
+    w = World(nb=4, max_blocks=8, max_seqs=4)
+    w.add(0, list(range(16)))
+    w.add(1, list(range(100, 116)))
+    w.add(2, list(range(200, 216)))
+    before = (list(w.m.ref), set(w.m.free), w.m.counts())
+    with pytest.raises(BM.NoBlocks):               # three new blocks needed, one free
+        w.m.append_step([0, 1, 2], [1, 2, 3])
+    assert (list(w.m.ref), set(w.m.free), w.m.counts()) == before
