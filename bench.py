@@ -62,6 +62,23 @@ def parse():
 # helpers
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The largest value of x over all ranks: the slowest replica's time."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_gbs(bytes_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job GB/s of `world` weak-scaling replicas: every rank moves the
+    same bytes, and the job ends with the slowest one."""
+    return world * bytes_per_rank / seconds / 1e9
+
+
 def peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -330,15 +347,12 @@ def run_ours(args, rank, world, local_rank):
     total_ms = ev[0][0].elapsed_time(ev[-1][2])
     attn_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     app_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev, world)
 
     dec_b = [wl.decode_bytes((args.warmup + k) % wl.steps) for k in range(args.steps)]
     app_b = wl.append_bytes()
     step_bytes = sum(dec_b) + args.steps * app_b
-    value = world * step_bytes / (total_ms * 1e-3) / 1e9
+    value = replica_gbs(step_bytes, total_ms * 1e-3, world)
     ms_per_step = total_ms / args.steps
     peak, peak_kind = peak_hbm()
     attn_avg_ms = statistics.mean(attn_ms)
@@ -389,11 +403,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step(args.warmup + k)
         te1 = time.perf_counter()
         e2e_s = te1 - te0
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e_value = world * step_bytes / e2e_s / 1e9
+    e2e_s = max_over_ranks(e2e_s, dev, world)
+    e2e_value = replica_gbs(step_bytes, e2e_s, world)
 
     status = pa.pa_device_status()
     if rank != 0:

@@ -1,0 +1,70 @@
+"""The multi-GPU path of the benchmark on the CPU: N independent replicas
+(the decode shards by sequence with no exchange), timed by the slowest rank.
+Runs world_size-2 process groups over gloo on 127.0.0.1; the GPU kernels are
+not involved, only the host logic that turns per-rank times into the job's
+figure, and the reference arm's rank handling under torchrun."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = [0.120, 0.135][rank]                 # rank 1 is the slow replica
+        slowest = bench.max_over_ranks(mine, torch.device("cpu"), world)
+        dist.barrier()
+        out[rank] = (slowest, bench.replica_gbs(717.18e6 * 64, slowest * 64, world))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_report_the_slowest_rank_and_the_summed_bytes():
+    port = _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1]
+    slowest, gbs = out[0]
+    assert slowest == pytest.approx(0.135)
+    assert gbs == pytest.approx(2 * 717.18e6 / 0.135 / 1e9)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(1.5, torch.device("cpu"), 1) == 1.5
+    assert bench.replica_gbs(1e9, 1.0, 1) == pytest.approx(1.0)
+
+
+@pytest.mark.slow
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
