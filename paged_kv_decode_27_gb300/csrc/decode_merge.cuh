@@ -28,13 +28,13 @@ __device__ __forceinline__ size_t query_row(const DecodeArgs& a, int s, int kvh,
   return (static_cast<size_t>(s) * a.q_len + i) * a.num_q_heads + kvh * G + h;
 }
 
-template <typename T, int W, int D, int NC = 8>
+template <typename T, int W, int D, int NC = 8, int NTHREADS = W * 32>
 __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float* red_o,
                                                 const float* red_m, const float* red_l, int G,
                                                 int s, int kvh, int split, int n_splits) {
   __shared__ int s_last;
   const int ncols = G * a.q_len;
-  for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+  for (int idx = threadIdx.x; idx < ncols * D; idx += NTHREADS) {
     const int c = idx / D;
     const int d = idx - c * D;
     float M = -INFINITY;
@@ -80,7 +80,7 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
   if (!s_last) return;
   T* out = static_cast<T*>(a.out);
   constexpr int kBatch = 8;   // partials whose loads are in flight together
-  for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+  for (int idx = threadIdx.x; idx < ncols * D; idx += NTHREADS) {
     const int c = idx / D;
     const int d = idx - c * D;
     const size_t qr = query_row(a, s, kvh, G, c);

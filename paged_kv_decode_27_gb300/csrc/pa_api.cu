@@ -441,7 +441,8 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
   CUtensorMap kmap, vmap;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
-  cudaError_t e = pa::launch_decode_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  cudaError_t e = q_len == 1 ? pa::launch_decode_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream))
+                             : pa::launch_verify_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return PA_OK;
 }

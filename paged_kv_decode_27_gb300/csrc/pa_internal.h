@@ -65,6 +65,11 @@ cudaError_t launch_append(void* k_pool, void* v_pool, const int64_t* slot_mappin
 cudaError_t launch_decode_tc(const DecodeArgs& a, int dtype, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream);
 
+// Verification attention (q_len > 1 query positions per sequence, bf16/fp16):
+// one consumer warp per 8 query columns over a CTA-shared ring of K/V stages.
+cudaError_t launch_verify_tc(const DecodeArgs& a, int dtype, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, cudaStream_t stream);
+
 // CUDA-core decode (any supported dtype; the fp32 path).
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t stream);
 
