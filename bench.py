@@ -298,13 +298,12 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty((S, hq, d), dtype=wl.dtype, device=dev)
     stream = torch.cuda.current_stream()
     max_splits = -(-((max_ctx + 15) // 16) // (part // 16))
-    launches_per_step = 2   # append_kv_kernel + decode_tc_kernel
+    launches_per_step = 1   # decode_tc_kernel with the step's append fused in (pa_decode_step)
 
     def step(i):
-        slots, kn, vn, q, ctx = dev_in[i % wl.steps]
-        pa.pa_append_kv(kp, vp, slots, kn, vn, stream=stream)
-        pa.pa_decode_attention(out, q, kp, vp, bt, ctx, wl.scale, max_context_len=max_ctx,
-                               partition_size=args.partition, workspace=ws, stream=stream)
+        _, kn, vn, q, ctx = dev_in[i % wl.steps]
+        pa.pa_decode_step(out, q, kp, vp, kn, vn, bt, ctx, wl.scale, max_context_len=max_ctx,
+                          partition_size=args.partition, workspace=ws, stream=stream)
 
     # untimed: >= 1 s of steps so the clock sampler sees the GPU under load, then W warm-ups
     sampler = ClockSampler(local_rank) if rank == 0 else None
@@ -325,18 +324,13 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
 
     # timed: exactly K steps, events on the launching stream around each call
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for k in range(args.steps):
-        t = args.warmup + k
-        slots, kn, vn, q, ctx = dev_in[t % wl.steps]
         ev[k][0].record(stream)
-        pa.pa_append_kv(kp, vp, slots, kn, vn, stream=stream)
+        step(args.warmup + k)
         ev[k][1].record(stream)
-        pa.pa_decode_attention(out, q, kp, vp, bt, ctx, wl.scale, max_context_len=max_ctx,
-                               partition_size=args.partition, workspace=ws, stream=stream)
-        ev[k][2].record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
@@ -344,9 +338,8 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         time.sleep(0.25)
         sampler.stop()
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    attn_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
-    app_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    attn_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     total_ms = max_over_ranks(total_ms, dev, world)
 
     dec_b = [wl.decode_bytes((args.warmup + k) % wl.steps) for k in range(args.steps)]
@@ -359,14 +352,11 @@ def run_ours(args, rank, world, local_rank):
     achieved = statistics.mean(dec_b) / (attn_avg_ms * 1e-3) / 1e9
     kv_ratio = statistics.mean(dec_b) / wl.decode_bytes(0)
 
-    # e2e through the public API with host buffers: pinned H2D of the step's
-    # inputs (q, new K/V, slots, context lengths, block tables), the two calls,
-    # D2H of the attention output, synchronised every step
-    # e2e through the public API with host buffers: each step's inputs (new-token slots, new K/V, q,
-    # context lengths, block tables) sit packed in one pinned host buffer and go to the device in one
-    # H2D copy; then the two calls, a D2H copy of the attention output, and a synchronise
+    # e2e through the public API with host buffers: each step's inputs (new K/V, q, context
+    # lengths, block tables) sit packed in one pinned host buffer and go to the device in one H2D
+    # copy; then the step call, a D2H copy of the attention output, and a synchronise
     def pack(st):
-        parts = [st.slot_mapping, st.k_new, st.v_new, st.q, st.context_lens, bt_cpu]
+        parts = [st.k_new, st.v_new, st.q, st.context_lens, bt_cpu]
         flat = [x.contiguous().view(torch.uint8).reshape(-1) for x in parts]
         pad = [(-f.numel()) % 16 for f in flat]   # keep every view 16-byte aligned
         buf = torch.cat([torch.cat([f, torch.zeros(p_, dtype=torch.uint8)]) for f, p_ in zip(flat, pad)])
@@ -379,17 +369,39 @@ def run_ours(args, rank, world, local_rank):
         n = int(torch.Size(shp).numel()) * torch.empty((), dtype=dt).element_size()
         views.append(d_buf[off:off + n].view(dt).view(shp))
         off += nb
-    d_slots, d_kn, d_vn, d_q, d_ctx, d_bt = views
+    d_kn, d_vn, d_q, d_ctx, d_bt = views
     out_host = torch.empty((S, hq, d), dtype=wl.dtype).pin_memory()
     h2d = packed[0][0].numel()
     d2h = out_host.numel() * out_host.element_size()
 
-    def e2e_step(t):
+    def enqueue(t, st):
         d_buf.copy_(packed[t % wl.steps][0], non_blocking=True)
-        pa.pa_append_kv(kp, vp, d_slots, d_kn, d_vn, stream=stream)
-        pa.pa_decode_attention(out, d_q, kp, vp, d_bt, d_ctx, wl.scale, max_context_len=max_ctx,
-                               partition_size=args.partition, workspace=ws, stream=stream)
+        pa.pa_decode_step(out, d_q, kp, vp, d_kn, d_vn, d_bt, d_ctx, wl.scale, max_context_len=max_ctx,
+                          partition_size=args.partition, workspace=ws, stream=st)
         out_host.copy_(out, non_blocking=True)
+
+    # The library allocates nothing and never synchronises, so a step (H2D of
+    # its packed inputs, the append + decode call, D2H of the output) can be captured in
+    # a CUDA graph once per input buffer and replayed: one launch per step.
+    graphs, e2e_mode = [], "eager"
+    if not args.quick:
+        try:
+            torch.cuda.synchronize()
+            for t in range(wl.steps):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    enqueue(t, torch.cuda.current_stream())
+                graphs.append(g)
+            e2e_mode = "cuda_graph"
+        except Exception as exc:   # capture unsupported here: time the eager calls instead
+            graphs, e2e_mode = [], f"eager ({type(exc).__name__})"
+            torch.cuda.synchronize()
+
+    def e2e_step(t):
+        if graphs:
+            graphs[t % wl.steps].replay()
+        else:
+            enqueue(t, stream)
         stream.synchronize()
     e2e_s = float("nan")
     if not args.quick:
@@ -416,15 +428,18 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "partition_tokens": part, "max_splits": max_splits,
                    "l2": "inputs larger than L2: ~726 MB of K/V read per step vs 129 MB L2, no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step": "pa_decode_step: each sequence's new token appended by the decode launch itself"},
         "pct_of_peak": value / peak,
         "decode_tokens_per_s": world * S * args.steps / (total_ms * 1e-3),
-        "attention_us": 1e3 * attn_avg_ms, "append_us": 1e3 * statistics.mean(app_ms),
+        "attention_us": 1e3 * attn_avg_ms, "append_us": None,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(kv_ratio),
-                     "kernel": "pa_decode_attention (decode_tc_kernel, split-K merge fused), CUDA events per call",
+                     "kernel": "pa_decode_step (decode_tc_kernel: append and split-K merge fused), "
+                               "CUDA events per call",
                      "peak_kind": f"{peak_kind} (STREAM-like copy, burst)"},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "mode": e2e_mode},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "device_status": status,
         "cpu_baseline": cpu,

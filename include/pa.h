@@ -176,6 +176,27 @@ PA_API int pa_decode_attention(void* out, const void* q, const void* k_pool, con
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_step -- one decode step in one launch: pa_append_kv of every
+ * sequence's new token followed by pa_decode_attention.
+ *
+ * In a decode step each sequence gains exactly one token, at position
+ * context_lens[s] - 1 (its slot comes from the block table, so no slot
+ * mapping is passed); k_new / v_new hold those tokens, [num_seqs][H_kv][D] in
+ * the pool dtype, 16-byte aligned.  The CTA that attends to a sequence's last
+ * partition writes the token (K and V, its KV head) into the pool before it
+ * reads that block, so the result equals pa_append_kv at those slots followed
+ * by pa_decode_attention, bit for bit, and the pool keeps the token for the
+ * next step.  A sequence with context_len 0 appends nothing.  Arguments,
+ * workspace and errors as pa_decode_attention, plus PA_ERR_INVALID for null or
+ * misaligned k_new / v_new.
+ */
+PA_API int pa_decode_step(void* out, const void* q, void* k_pool, void* v_pool, const void* k_new,
+                          const void* v_new, const int32_t* block_tables, const int32_t* context_lens,
+                          float scale, int num_seqs, int num_q_heads, int max_blocks_per_seq,
+                          int max_context_len, int partition_size, const pa_pool_desc* pool,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_verify_attention -- attention for the verification pass of speculative
  * decoding: q_len query tokens per sequence (the last accepted token and the
  * q_len - 1 drafted ones, "LLM Inference Server", Batched Scheduling &

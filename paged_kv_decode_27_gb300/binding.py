@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_attention.restype = i32
     L.pa_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, pdesc,
                                       vp, sz, vp]
+    L.pa_decode_step.restype = i32
+    L.pa_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, pdesc, vp, sz, vp]
     L.pa_prefill_attention.restype = i32
     L.pa_prefill_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32,
                                        pdesc, vp]
@@ -267,6 +269,37 @@ def pa_verify_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor
                                  _ptr(context_lens), float(scale), S, ql, hq, int(block_tables.shape[1]),
                                  int(max_context_len), int(partition_size), ctypes.byref(desc), _ptr(workspace),
                                  int(ws_bytes), _stream(stream)))
+
+
+def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                   k_new: torch.Tensor, v_new: torch.Tensor, block_tables: torch.Tensor,
+                   context_lens: torch.Tensor, scale: float, max_context_len: int, partition_size: int = 0,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Append each sequence's new token (k_new / v_new [S][H_kv][D], at
+    position context_lens[s] - 1) and decode, in one launch."""
+    desc = _pools(k_pool, v_pool)
+    for n, t in (("out", out), ("q", q), ("k_new", k_new), ("v_new", v_new), ("block_tables", block_tables),
+                 ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 3 and q.shape[2] == k_pool.shape[3], "q must be [S][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype == k_pool.dtype, "out/q shape or dtype mismatch")
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    shape = (S, k_pool.shape[1], k_pool.shape[3])
+    _need(tuple(k_new.shape) == shape and tuple(v_new.shape) == shape, f"k_new/v_new must be {shape}")
+    _need(k_new.dtype == v_new.dtype == k_pool.dtype, "k_new/v_new dtype must match the pool")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
+    L = load_library()
+    if workspace is None:
+        need = pa_decode_workspace_size(S, hq, max_context_len, k_pool, partition_size)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.pa_decode_step(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+                            _ptr(block_tables), _ptr(context_lens), float(scale), S, hq, int(block_tables.shape[1]),
+                            int(max_context_len), int(partition_size), ctypes.byref(desc), _ptr(workspace),
+                            int(ws_bytes), _stream(stream)))
 
 
 def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

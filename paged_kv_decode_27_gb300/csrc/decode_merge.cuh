@@ -130,6 +130,31 @@ __device__ __forceinline__ void store_zero_rows(const DecodeArgs& a, int G, int 
   }
 }
 
+// Append fused into a decode step: the CTA that holds a sequence's last
+// partition writes the step's new token (position ctx - 1) of its KV head
+// into the pool, K and V, 16 bytes per thread.  The caller orders the write
+// before its own reads of that block (a CTA barrier, plus a generic-to-async
+// proxy fence when the reads are TMA copies).
+template <typename T, int D>
+__device__ __forceinline__ void write_step_token(const DecodeArgs& a, int s, int kvh, int ctx, int nthreads) {
+  constexpr int CH = D * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row
+  const int pos = ctx - 1;
+  const int id = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / kBlock);
+  if (id < 0 || id >= a.num_blocks) {
+    if (threadIdx.x == 0) flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+    return;
+  }
+  const size_t row = (static_cast<size_t>(id) * a.num_kv_heads + kvh) * kBlock + pos % kBlock;
+  const size_t src = static_cast<size_t>(s) * a.num_kv_heads + kvh;
+  for (int c = threadIdx.x; c < 2 * CH; c += nthreads) {
+    const bool is_v = c >= CH;
+    const int cc = is_v ? c - CH : c;
+    const uint4* from = static_cast<const uint4*>(is_v ? a.v_new : a.k_new) + src * CH + cc;
+    uint4* to = static_cast<uint4*>(const_cast<void*>(is_v ? a.v_pool : a.k_pool)) + row * CH + cc;
+    *to = __ldg(from);
+  }
+}
+
 // Context length as the kernels use it: clamped to what the block table can
 // address, with the clamp recorded in the status word.
 __device__ __forceinline__ int checked_context(const DecodeArgs& a, int s, bool report) {

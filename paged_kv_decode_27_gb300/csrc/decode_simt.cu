@@ -60,6 +60,10 @@ __global__ void __launch_bounds__(W * 32) decode_simt_kernel(const DecodeArgs a)
     return;
   }
   if (split >= n_splits) return;
+  if (a.k_new != nullptr && split == n_splits - 1) {   // decode step with the append fused in
+    write_step_token<T, D>(a, s, kvh, ctx, W * 32);
+    __syncthreads();
+  }
   const int blk0 = split * a.part_blocks;
   const int nblk = min(a.part_blocks, nblk_seq - blk0);
 

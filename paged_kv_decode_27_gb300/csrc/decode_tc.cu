@@ -74,6 +74,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     return;
   }
   if (split >= n_splits) return;
+  if (a.k_new != nullptr && split == n_splits - 1) {
+    // decode step with the append fused in: write this step's token, then let
+    // the TMA copies below (async proxy) see it
+    write_step_token<T, D>(a, s, kvh, ctx, W * 32);
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+  }
   const int blk0 = split * a.part_blocks;
   const int nblk = min(a.part_blocks, nblk_seq - blk0);
   const int nb_w = nblk > warp ? (nblk - warp + W - 1) / W : 0;   // <= 32 (host limit)

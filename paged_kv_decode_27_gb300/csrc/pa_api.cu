@@ -292,12 +292,42 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_context_l
   return ws_layout(num_seqs, num_q_heads, ms, pool->head_dim).total;
 }
 
+namespace {
+int decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool, const void* k_new,
+                const void* v_new, const int32_t* block_tables, const int32_t* context_lens, float scale,
+                int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_context_len, int partition_size,
+                const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream);
+}
+
 int pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
                         const int32_t* block_tables, const int32_t* context_lens, float scale,
                         int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_context_len,
                         int partition_size, const pa_pool_desc* pool, void* workspace,
                         size_t workspace_bytes, void* stream) {
   t_err.clear();
+  return decode_impl(out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens, scale, num_seqs,
+                     num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool, workspace,
+                     workspace_bytes, stream);
+}
+
+int pa_decode_step(void* out, const void* q, void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                   const int32_t* block_tables, const int32_t* context_lens, float scale, int num_seqs,
+                   int num_q_heads, int max_blocks_per_seq, int max_context_len, int partition_size,
+                   const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  if (num_seqs > 0 && (!k_new || !v_new)) return fail(PA_ERR_INVALID, "null k_new / v_new");
+  if (num_seqs > 0 && (!aligned16(k_new) || !aligned16(v_new)))
+    return fail(PA_ERR_INVALID, "k_new / v_new must be 16-byte aligned");
+  return decode_impl(out, q, k_pool, v_pool, k_new, v_new, block_tables, context_lens, scale, num_seqs,
+                     num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool, workspace,
+                     workspace_bytes, stream);
+}
+
+namespace {
+int decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool, const void* k_new,
+                const void* v_new, const int32_t* block_tables, const int32_t* context_lens, float scale,
+                int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_context_len, int partition_size,
+                const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool);
   if (rc != PA_OK) return rc;
   if ((rc = reject_int8(pool)) != PA_OK) return rc;
@@ -348,6 +378,8 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
   a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
   a.status = status;
   a.q_len = 1;
+  a.k_new = k_new;
+  a.v_new = v_new;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -362,6 +394,7 @@ int pa_decode_attention(void* out, const void* q, const void* k_pool, const void
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PA_OK;
 }
+}  // namespace
 
 size_t pa_verify_workspace_size(int num_seqs, int q_len, int num_q_heads, int max_context_len, int partition_size,
                                 const pa_pool_desc* pool) {

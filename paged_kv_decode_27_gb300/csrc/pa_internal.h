@@ -34,6 +34,10 @@ struct DecodeArgs {
   const float* k_scales;   // INT8 cache only: [N_blk][H_kv][16] row scales
   const float* v_scales;
   int q_len;               // query positions per sequence: 1 for decode, K+1 to verify K drafts
+  // decode step with the append fused in: the new token of each sequence
+  // ([S][H_kv][D] rows, written at position context - 1); null otherwise
+  const void* k_new;
+  const void* v_new;
 };
 
 struct PrefillArgs {

@@ -208,3 +208,12 @@ def test_rope_entry_points_validate_on_the_host(lib):
     assert app(T=0) == B.PA_OK
     assert lib.pa_apply_rope(f, f, 4, 8, 128, B.PA_I8, f, 100, None) == B.PA_ERR_UNSUPPORTED
     assert lib.pa_apply_rope(ctypes.c_void_p(FAKE + 8), f, 4, 8, 128, B.PA_BF16, f, 100, None) == B.PA_ERR_INVALID
+
+
+def test_decode_step_validates_on_the_host(lib):
+    f = ctypes.c_void_p(FAKE)
+    call = lambda kn=f, d=_desc(): lib.pa_decode_step(f, f, f, f, kn, f, f, f, 0.1, 4, 32, 8, 100, 512,
+                                                      ctypes.byref(d), None, 0, None)
+    assert call(kn=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
+    assert call(kn=ctypes.c_void_p(FAKE + 8)) == B.PA_ERR_INVALID
+    assert call(d=_desc(dt=B.PA_I8)) == B.PA_ERR_INVALID
