@@ -28,6 +28,52 @@ __device__ __forceinline__ size_t query_row(const DecodeArgs& a, int s, int kvh,
   return (static_cast<size_t>(s) * a.q_len + i) * a.num_q_heads + kvh * G + h;
 }
 
+// Log-sum-exp merge of the n_parts split-K partials of (sequence s, KV head
+// kvh) into the output rows: with M = max_p lse_p and w_p = 2^(lse_p - M),
+// out = sum_p w_p o_p / sum_p w_p -- the softmax over the whole context.
+// Threads tid = 0 .. nthreads-1 share the G * q_len * D outputs.
+template <typename T, int D>
+__device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int s, int kvh, int G, int n_parts,
+                                                     int tid, int nthreads) {
+  T* out = static_cast<T*>(a.out);
+  const int ncols = G * a.q_len;
+  constexpr int kBatch = 8;   // partials whose loads are in flight together
+  for (int idx = tid; idx < ncols * D; idx += nthreads) {
+    const int c = idx / D;
+    const int d = idx - c * D;
+    const size_t qr = query_row(a, s, kvh, G, c);
+    const size_t row0 = qr * a.max_splits;
+    // a running max over batches of partitions; each batch issues all of its
+    // loads before any arithmetic, so the merge costs ~one memory latency per
+    // batch instead of one per partition
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    for (int p0 = 0; p0 < n_parts; p0 += kBatch) {
+      float lp[kBatch], op[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const bool in = p0 + k < n_parts;
+        lp[k] = in ? __ldcg(a.ws_lse + row0 + p0 + k) : -INFINITY;
+        op[k] = in ? __ldcg(a.ws_o + (row0 + p0 + k) * D + d) : 0.f;
+      }
+      float mb = M;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, lp[k]);
+      if (mb == -INFINITY) continue;
+      const float r = exp2f(M - mb);      // 0 while M is still -inf
+      L *= r;
+      O *= r;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float w = exp2f(lp[k] - mb);   // 0 for empty partitions
+        L += w;
+        O = fmaf(w, op[k], O);
+      }
+      M = mb;
+    }
+    out[qr * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
+  }
+}
+
 template <typename T, int W, int D, int NC = 8, int NTHREADS = W * 32>
 __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float* red_o,
                                                 const float* red_m, const float* red_l, int G,
@@ -78,42 +124,7 @@ __device__ __forceinline__ void cta_merge_store(const DecodeArgs& a, const float
   }
   __syncthreads();
   if (!s_last) return;
-  T* out = static_cast<T*>(a.out);
-  constexpr int kBatch = 8;   // partials whose loads are in flight together
-  for (int idx = threadIdx.x; idx < ncols * D; idx += NTHREADS) {
-    const int c = idx / D;
-    const int d = idx - c * D;
-    const size_t qr = query_row(a, s, kvh, G, c);
-    const size_t row0 = qr * a.max_splits;
-    // a running max over batches of partitions; each batch issues all of its
-    // loads before any arithmetic, so the merge costs ~one memory latency per
-    // batch instead of one per partition
-    float M = -INFINITY, L = 0.f, O = 0.f;
-    for (int p0 = 0; p0 < n_splits; p0 += kBatch) {
-      float lp[kBatch], op[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const bool in = p0 + k < n_splits;
-        lp[k] = in ? __ldcg(a.ws_lse + row0 + p0 + k) : -INFINITY;
-        op[k] = in ? __ldcg(a.ws_o + (row0 + p0 + k) * D + d) : 0.f;
-      }
-      float mb = M;
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, lp[k]);
-      if (mb == -INFINITY) continue;
-      const float r = exp2f(M - mb);      // 0 while M is still -inf
-      L *= r;
-      O *= r;
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const float w = exp2f(lp[k] - mb);   // 0 for empty partitions
-        L += w;
-        O = fmaf(w, op[k], O);
-      }
-      M = mb;
-    }
-    out[qr * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
-  }
+  merge_split_partials<T, D>(a, s, kvh, G, n_splits, threadIdx.x, NTHREADS);
   // leave the counter at zero for the next call on this workspace
   if (threadIdx.x == 0) *counter = 0;
 }

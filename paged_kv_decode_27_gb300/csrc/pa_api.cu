@@ -125,6 +125,16 @@ int max_splits_for(int max_context_len, int part_blocks) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Verification on the tensor-core kernel: head dim 128 and more than one query position.
+bool verify_on_umma(int q_len, int head_dim) { return q_len > 1 && head_dim == 128; }
+
+// Partial-output slots per query row of a verify call: the split-K partitions of
+// the mma.sync kernels, or the stream-K segments of the tensor-core kernel.
+int verify_slots(int q_len, int head_dim, int max_context_len, int part_blocks) {
+  return verify_on_umma(q_len, head_dim) ? pa::verify_umma_slots(max_context_len, part_blocks)
+                                         : max_splits_for(max_context_len, part_blocks);
+}
+
 // [counters: kCounterBytes][partial outputs: rows x D fp32][partial lse: rows fp32]
 struct WsLayout {
   size_t o_off, lse_off, total;
@@ -406,7 +416,7 @@ size_t pa_verify_workspace_size(int num_seqs, int q_len, int num_q_heads, int ma
     return 0;
   }
   const int p = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
-  const int ms = max_splits_for(max_context_len, p / PA_BLOCK_SIZE);
+  const int ms = verify_slots(q_len, pool->head_dim, max_context_len, p / PA_BLOCK_SIZE);
   return ws_layout(num_seqs * q_len, num_q_heads, ms, pool->head_dim).total;
 }
 
@@ -435,7 +445,7 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
 
   const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
   const int part_blocks = part / PA_BLOCK_SIZE;
-  const int max_splits = max_splits_for(max_context_len, part_blocks);
+  const int max_splits = verify_slots(q_len, pool->head_dim, max_context_len, part_blocks);
   const WsLayout ws = ws_layout(num_seqs * q_len, num_q_heads, max_splits, pool->head_dim);
   if (ws.total > 0 && static_cast<long long>(num_seqs) * pool->num_kv_heads > kMaxCounters)
     return fail(PA_ERR_UNSUPPORTED, "split-K over more than %d (sequence, KV head) pairs in one call",
@@ -474,8 +484,10 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
   CUtensorMap kmap, vmap;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
-  cudaError_t e = q_len == 1 ? pa::launch_decode_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream))
-                             : pa::launch_verify_tc(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = q_len == 1                                 ? pa::launch_decode_tc(a, pool->dtype, kmap, vmap, st)
+                  : verify_on_umma(q_len, pool->head_dim) ? pa::launch_verify_umma(a, pool->dtype, kmap, vmap, st)
+                                                            : pa::launch_verify_tc(a, pool->dtype, kmap, vmap, st);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return PA_OK;
 }

@@ -74,6 +74,14 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int dtype, const CUtensorMap& 
 cudaError_t launch_verify_tc(const DecodeArgs& a, int dtype, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream);
 
+// Verification attention on the tensor cores (tcgen05), head dim 128, q_len > 1:
+// a persistent stream-K launch, one CTA per SM.  a.part_blocks / 8 is the
+// shortest range of 128-token tiles a CTA takes; a.max_splits must be
+// verify_umma_slots(max_context_len, part_blocks) (partials per output row).
+cudaError_t launch_verify_umma(const DecodeArgs& a, int dtype, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t stream);
+int verify_umma_slots(int max_context_len, int part_blocks);
+
 // CUDA-core decode (any supported dtype; the fp32 path).
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, cudaStream_t stream);
 

@@ -189,9 +189,17 @@ def test_verify_validates_on_the_host(lib):
     d = _desc()
     assert lib.pa_verify_workspace_size(64, 1, 32, 8224, 0, ctypes.byref(d)) == \
         lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(d))
-    rows = 64 * 5 * 32 * 9
+    # head dim 128, q_len > 1: the tensor-core kernel keeps one partial per stream-K
+    # segment; with 1024-token partitions a segment spans >= 8 tiles of 128 tokens, so
+    # a context of 8224 tokens (65 tiles) meets at most ceil(65 / 8) + 1 = 10 segments
+    rows = 64 * 5 * 32 * 10
     assert lib.pa_verify_workspace_size(64, 5, 32, 8224, 0, ctypes.byref(d)) == \
         ((256 * 1024 + rows * 128 * 4 + 255) // 256) * 256 + rows * 4
+    # head dim 64 stays on the mma.sync kernel: one partial per 1024-token partition
+    d64 = _desc(d=64)
+    rows = 64 * 5 * 32 * 9
+    assert lib.pa_verify_workspace_size(64, 5, 32, 8224, 0, ctypes.byref(d64)) == \
+        ((256 * 1024 + rows * 64 * 4 + 255) // 256) * 256 + rows * 4
 
 
 def test_rope_entry_points_validate_on_the_host(lib):
