@@ -20,22 +20,23 @@
 // over several CTAs leaves one normalised partial per segment and the CTA that
 // finishes its segment last merges them by log-sum-exp (decode_merge.cuh).
 //
-// One CTA per SM, eleven warps with fixed roles:
+// One CTA per SM, twelve warps with fixed roles:
 //   warps 0-3  softmax: thread t owns token row t of S^T (tensor memory lane
 //              t).  The softmax reference of each column is shared by the CTA
 //              and raised lazily (only when a score exceeds it by 2^8; a CTA-
 //              wide vote decides, a transpose reduction gives the column
 //              maxima).  P^T goes to shared memory in the K-major layout the
 //              second product reads; a raise rescales O^T in tensor memory.
-//   warps 4-7  epilogue: thread d owns head-dim row d of O^T.  It loads the
-//              next segment's q into shared memory ahead of time, normalises
-//              and stores each finished segment, and runs the split-K merge;
-//              none of this holds up the tiles of the next segment.
-//   warps 8/10 TMA producers of K tiles (2 stages) and V tiles (3 stages) of
+//   warps 4-7  epilogue: thread d owns head-dim row d of O^T.  It normalises
+//              and stores each finished segment and runs the split-K merge;
+//              none of this holds up the tiles of the next segments.
+//   warps 8/10 TMA producers of K tiles and V tiles (3 stages each) of
 //              8 pool blocks through the block table; blocks past the context
-//              or with an id outside the pool are read as zeros.
-//   warp 9     MMA issuer: S^T of tile j, then O^T += V^T P of tile j - 1, so
-//              the tensor cores compute while the softmax of tile j runs.
+//              or with an id outside the pool are read as zeros.  The K warp
+//              also stages each segment's q, ahead of its first K tile.
+//   warps 9/11 MMA issuers: S^T of tile j (warp 9) and O^T += V^T P of tile j
+//              (warp 11), so the scores of the next tile are computed while the
+//              softmax of this one runs.
 // Tensor memory: two S^T buffers and two O^T buffers of NC columns (O^T
 // alternates by segment so the epilogue of one overlaps the next).
 //
@@ -58,23 +59,22 @@ constexpr int kTileBlocks = kTok / kBlock;     // 8 pool blocks
 constexpr int kDim = 128;                      // head dim (MMA M of O^T)
 constexpr int kStrip = kTok * 128;             // one 64-column strip of a K or V tile
 constexpr int kTileBytes = 2 * kStrip;         // 32 KB
-constexpr int kKStages = 2;
+constexpr int kKStages = 3;
 constexpr int kVStages = 3;
-constexpr int kUThreads = 352;
+constexpr int kUThreads = 384;
 constexpr float kLazyU = 8.f;                  // log2 headroom of the softmax reference
 
 template <int NC>
 struct VLayout {
   static constexpr int QSTRIP = NC * 128;      // one 64-column strip of q (NC rows)
   static constexpr int QBYTES = 2 * QSTRIP;
-  static constexpr int PSTRIP = NC * 128;      // one 64-token strip of P^T (NC rows)
-  static constexpr int PBYTES = 2 * PSTRIP;
+  static constexpr int PBYTES = kTok * NC * 2; // P: 128 token rows of NC columns (one buffer)
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + kKStages * kTileBytes;
   static constexpr int Q_OFF = V_OFF + kVStages * kTileBytes;
   static constexpr int P_OFF = Q_OFF + 2 * QBYTES;
-  static constexpr int SMEM = P_OFF + 2 * PBYTES;
-  static constexpr uint32_t TMEM_COLS = 4 * NC;   // S^T x2, O^T x2 (a power of two >= 32)
+  static constexpr int SMEM = P_OFF + PBYTES;
+  static constexpr uint32_t TMEM_COLS = NC == 32 ? 256 : 128;   // S^T x2, O^T x3 (a power of two)
 };
 
 template <typename T>
@@ -101,21 +101,15 @@ __device__ __forceinline__ bool cta_any(int barrier_id, bool v) {
   return r != 0;
 }
 
-// Bounded wait that lets the thread sleep (up to 20 us per try, woken when the
-// phase completes): for roles whose waits are long and off the critical path,
-// so they take no issue slots from the softmax warps while they wait.
+// Bounded wait for roles whose waits are long and off the critical path: between
+// polls the thread naps ~0.1 us, so it takes few issue slots from the softmax warps
+// and wakes at most that late.
 __device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(20000u)
-        : "memory");
-    if (ok) return true;
+    __nanosleep(100);
+    if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -213,8 +207,17 @@ __device__ __forceinline__ long long owner_of(long long x, long long T, int geff
 
 __device__ __forceinline__ int tiles_of(int ctx) { return (ctx + kTok - 1) / kTok; }
 
+// Contexts of the CTA's first kCtxCache sequences, cached in shared memory: every
+// role walks the same sequences, and a global load per new sequence would stall it.
+constexpr int kCtxCache = 64;
+
+__device__ __forceinline__ int walk_context(const DecodeArgs& a, const int* cache, int s0, int s) {
+  return s - s0 < kCtxCache ? cache[s - s0] : checked_context(a, s, false);
+}
+
 // Next segment of the walk; false when the CTA's range is done.
-__device__ __forceinline__ bool next_segment(const DecodeArgs& a, Walk& w, long long T, int geff, Segment& g) {
+__device__ __forceinline__ bool next_segment(const DecodeArgs& a, Walk& w, long long T, int geff, Segment& g,
+                                             const int* cache, int s0) {
   if (w.left <= 0) return false;
   while (w.nt == 0 || w.j >= w.nt) {   // the walk never rests on an empty or finished sequence
     if (w.nt > 0 && w.j >= w.nt) {
@@ -226,7 +229,7 @@ __device__ __forceinline__ bool next_segment(const DecodeArgs& a, Walk& w, long 
     w.j = 0;
     ++w.s;
     if (w.s >= a.num_seqs) return false;
-    w.ctx = checked_context(a, w.s, false);
+    w.ctx = walk_context(a, cache, s0, w.s);
     w.nt = tiles_of(w.ctx);
   }
   g.s = w.s;
@@ -256,16 +259,17 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   constexpr int D = kDim;
 
   extern __shared__ uint8_t smem_raw[];
-  // kfull[2] kempty[2] vfull[3] vempty[3] qfull[2] qempty[2] sfull[2] sfree[2]
-  // pfull[2] pfree[2] ofull[2] ofree[2] stfull[2] stfree[2] final
-  __shared__ __align__(8) uint64_t bars[31];
+  // kfull[3] kempty[3] vfull[3] vempty[3] qfull[2] qempty[2] sfull[2] sfree[2]
+  // pfull[2] pfree[2] ofull[3] ofree[3] stfull[3] stfree[3] final
+  __shared__ __align__(8) uint64_t bars[37];
   __shared__ float red_sh[4][NC];              // column maxima of a raise, per softmax warp
   // The CTA's column references, alternating by raise (-inf while a column has none).
   __shared__ float mu_sh[2][NC];
-  __shared__ float st_l[2][4][NC];             // per segment: column sums of each softmax warp
-  __shared__ float st_m[2][NC];                // per segment: column references
+  __shared__ float st_l[3][4][NC];             // per segment: column sums of each softmax warp
+  __shared__ float st_m[3][NC];                // per segment: column references
   __shared__ long long walk_sh[3];             // start base, tiles left, total tiles
   __shared__ int walk_i[4];                    // s, kvh, j, geff
+  __shared__ int ctx_sh[kCtxCache];            // contexts of sequences walk_i[0] ...
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
   __shared__ int last_sh;
@@ -284,20 +288,20 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
   const uint32_t bar0 = smem_u32(&bars[0]);
   auto kfull = [&](int i) { return bar0 + 8u * i; };
-  auto kempty = [&](int i) { return bar0 + 16u + 8u * i; };
-  auto vfull = [&](int i) { return bar0 + 32u + 8u * i; };
-  auto vempty = [&](int i) { return bar0 + 56u + 8u * i; };
-  auto qfull = [&](int i) { return bar0 + 80u + 8u * i; };
-  auto qempty = [&](int i) { return bar0 + 96u + 8u * i; };
-  auto sfull = [&](int i) { return bar0 + 112u + 8u * i; };
-  auto sfree = [&](int i) { return bar0 + 128u + 8u * i; };
-  auto pfull = [&](int i) { return bar0 + 144u + 8u * i; };
-  auto pfree = [&](int i) { return bar0 + 160u + 8u * i; };
-  auto ofull = [&](int i) { return bar0 + 176u + 8u * i; };
-  auto ofree = [&](int i) { return bar0 + 192u + 8u * i; };
-  auto stfull = [&](int i) { return bar0 + 208u + 8u * i; };
-  auto stfree = [&](int i) { return bar0 + 224u + 8u * i; };
-  const uint32_t final_bar = bar0 + 240u;
+  auto kempty = [&](int i) { return bar0 + 24u + 8u * i; };
+  auto vfull = [&](int i) { return bar0 + 48u + 8u * i; };
+  auto vempty = [&](int i) { return bar0 + 72u + 8u * i; };
+  auto qfull = [&](int i) { return bar0 + 96u + 8u * i; };
+  auto qempty = [&](int i) { return bar0 + 112u + 8u * i; };
+  auto sfull = [&](int i) { return bar0 + 128u + 8u * i; };
+  auto sfree = [&](int i) { return bar0 + 144u + 8u * i; };
+  auto pfull = [&](int i) { return bar0 + 160u + 8u * i; };
+  auto pfree = [&](int i) { return bar0 + 176u + 8u * i; };
+  auto ofull = [&](int i) { return bar0 + 192u + 8u * i; };
+  auto ofree = [&](int i) { return bar0 + 216u + 8u * i; };
+  auto stfull = [&](int i) { return bar0 + 240u + 8u * i; };
+  auto stfree = [&](int i) { return bar0 + 264u + 8u * i; };
+  const uint32_t final_bar = bar0 + 288u;
 
   grid_dependency_wait();   // the cache and the queries come from the kernels before us
 
@@ -311,18 +315,20 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       mbar_init(vempty(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(qfull(i), 4);
+      mbar_init(qfull(i), 1);
       mbar_init(qempty(i), 1);
       mbar_init(sfull(i), 1);
       mbar_init(sfree(i), 4);
       mbar_init(pfull(i), 4);
       mbar_init(pfree(i), 1);
+    }
+    for (int i = 0; i < 3; ++i) {
       mbar_init(ofull(i), 1);
       mbar_init(ofree(i), 4);
       mbar_init(stfull(i), 4);
       mbar_init(stfree(i), 4);
     }
-    mbar_init(final_bar, 1);
+    mbar_init(final_bar, 2);
     fence_barrier_init();
     abort_sh = 0;
   }
@@ -373,6 +379,8 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       }
       pre += __shfl_sync(0xffffffffu, incl, 31);
     }
+    for (int k = lane; k < kCtxCache; k += 32)
+      ctx_sh[k] = fs + k < a.num_seqs ? checked_context(a, fs + k, false) : 0;
     if (lane == 0) {
       walk_sh[0] = fbase;
       walk_sh[1] = end - start;
@@ -400,7 +408,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     w.j = walk_i[2];
     w.base = walk_sh[0];
     w.left = walk_sh[1];
-    w.ctx = w.s < a.num_seqs ? checked_context(a, w.s, false) : 0;
+    w.ctx = w.s < a.num_seqs ? ctx_sh[0] : 0;
     w.nt = tiles_of(w.ctx);
     return w;
   };
@@ -413,7 +421,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   const uint32_t id_s = umma_idesc_f16(kTok, NC, kBf16, false, false);
   const uint32_t id_o = umma_idesc_f16(kDim, NC, kBf16, true, true);
   const uint32_t tS = tmem;                 // S^T buffers: columns [0, 2 NC)
-  const uint32_t tO = tmem + 2 * NC;        // O^T buffers: columns [2 NC, 4 NC)
+  const uint32_t tO = tmem + 2 * NC;        // O^T buffers: columns [2 NC, 5 NC), by segment % 3
 
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------- TMA producers: K (warp 8), V (warp 10)
@@ -428,9 +436,42 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const int oob_row = a.num_blocks * H * kBlock;   // rows past the pool read as zero
     Walk w = make_walk();
     Segment g;
-    int J = 0;
+    int J = 0, I = 0;
     bool ok = true;
-    while (ok && next_segment(a, w, ntot, geff, g)) {
+    while (ok && next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+      if (isk) {
+        // the segment's q, K-major and 128-byte swizzled, once segment I - 2's scores are done
+        const int qb = I & 1;
+        ok = I < 2 || waiti(qempty(qb), ((I >> 1) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const uint32_t qbase = sQ + qb * L::QBYTES;
+        const T* qg = static_cast<const T*>(a.q);
+        uint4 v[NC / 2];
+#pragma unroll
+        for (int k = 0; k < NC / 2; ++k) {   // all loads first: one memory latency
+          const int idx = lane + 32 * k;
+          const int c = idx >> 4;
+          v[k] = c < NQ ? __ldg(reinterpret_cast<const uint4*>(qg + query_row(a, g.s, g.kvh, G, c) * D) + (idx & 15))
+                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < NC / 2; ++k) {
+          const int idx = lane + 32 * k;
+          const int c = idx >> 4;
+          const int cc = idx & 15;
+          const uint32_t dst = qbase + (cc >> 3) * L::QSTRIP + c * 128 + (((cc & 7) ^ (c & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v[k].x), "r"(v[k].y), "r"(v[k].z),
+                       "r"(v[k].w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qfull(qb));
+      }
+      ++I;
       for (int jt = g.j0; jt < g.j0 + g.ntiles; ++jt) {
         // block rows of the tile (looked up before the stage wait, which hides the load)
         int y = oob_row;
@@ -465,88 +506,82 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     if (lane == 0)
       for (int j = J - nst < 0 ? 0 : J - nst; j < J; ++j)
         mbar_wait_bounded(isk ? kfull(j % nst) : vfull(j % nst), (j / nst) & 1, 100000000ull);
-  } else if (warp == 9) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == 9 || warp == 11) {
+    // --------------------------------------------------- MMA issuers: S^T (warp 9), O^T (warp 11)
+    // Two issuing warps: issuing stalls while the tensor pipe is busy, and the next
+    // tile's scores must not wait behind the previous tile's output product.
+    const bool is_s = warp == 9;
     Walk w = make_walk();
     Segment g;
     int J = 0, I = 0;
     bool ok = true;
-    // the O^T product of the previous tile, issued after the next tile's S^T
-    bool pend = false;
-    int pJ = 0, pI = 0;
-    bool pfirst = false, plast = false;
-    auto issue_pv = [&]() -> bool {
-      const int vs = pJ % kVStages;
-      const int pb = pJ & 1;
-      const int ob = pI & 1;
-      bool k = waitb(vfull(vs), (pJ / kVStages) & 1) && waitb(pfull(pb), (pJ >> 1) & 1);
-      if (k && pfirst && pI >= 2) k = waitb(ofree(ob), ((pI >> 1) - 1) & 1);
-      if (!__all_sync(0xffffffffu, k)) return false;
-      tc_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t vbase = sV + vs * kTileBytes;
-        const uint32_t pbase = sP + pb * L::PBYTES;
-#pragma unroll
-        for (int kk = 0; kk < kTok / 16; ++kk) {
-          const uint64_t da = umma_desc_sw128(vbase + kk * 2048, kStrip, 1024);
-          // P: MN-major, 16 tokens = two swizzle atoms of 8 rows x NC columns
-          const uint64_t db = umma_desc_mn_t<NC>(pbase + kk * (16 * NC * 2), 8 * NC * 2);
-          umma_f16(tO + ob * NC, da, db, id_o, (pfirst && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(pfree(pb));
-        umma_commit(vempty(vs));
-        if (plast) umma_commit(ofull(ob));
-      }
-      __syncwarp();
-      return true;
-    };
-    while (ok && next_segment(a, w, ntot, geff, g)) {
+    while (ok && next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
       const int qb = I & 1;
-      ok = waitb(qfull(qb), (I >> 1) & 1);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
+      const int ob = I % 3;
+      if (is_s) {
+        ok = waitb(qfull(qb), (I >> 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
       }
-      for (int t = 0; t < g.ntiles; ++t) {
-        const int ks = J % kKStages;
-        const int sb = J & 1;
-        bool k = waitb(kfull(ks), (J / kKStages) & 1);
-        if (k && J >= 2) k = waitb(sfree(sb), ((J >> 1) - 1) & 1);
-        if (!__all_sync(0xffffffffu, k)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (lane == 0) {
-          const uint32_t kbase = sK + ks * kTileBytes;
-          const uint32_t qbase = sQ + qb * L::QBYTES;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t da = umma_desc_sw128(kbase + (kk >> 2) * kStrip + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = umma_desc_sw128(qbase + (kk >> 2) * L::QSTRIP + (kk & 3) * 32, 16, 1024);
-            umma_f16(tS + sb * NC, da, db, id_s, kk > 0 ? 1u : 0u);
+      for (int t = 0; t < g.ntiles; ++t, ++J) {
+        if (is_s) {
+          // S^T_J = K_J q^T once K_J has landed and the softmax has read S_{J-2}
+          const int ks = J % kKStages;
+          const int sb = J & 1;
+          bool k = waitb(kfull(ks), (J / kKStages) & 1);
+          if (k && J >= 2) k = waitb(sfree(sb), ((J >> 1) - 1) & 1);
+          if (!__all_sync(0xffffffffu, k)) {
+            ok = false;
+            break;
           }
-          umma_commit(sfull(sb));
-          umma_commit(kempty(ks));
-          if (t == g.ntiles - 1) umma_commit(qempty(qb));
+          tc_fence_after_sync();
+          if (lane == 0) {
+            const uint64_t da0 = umma_desc_sw128(sK + ks * kTileBytes, 16, 1024);
+            const uint64_t db0 = umma_desc_sw128(sQ + qb * L::QBYTES, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {   // k-step kk: strip kk / 4, 32 bytes in per step
+              const uint64_t da = da0 + static_cast<uint64_t>(((kk >> 2) * kStrip + (kk & 3) * 32) >> 4);
+              const uint64_t db = db0 + static_cast<uint64_t>(((kk >> 2) * L::QSTRIP + (kk & 3) * 32) >> 4);
+              umma_f16(tS + sb * NC, da, db, id_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(sfull(sb));
+            umma_commit(kempty(ks));
+            if (t == g.ntiles - 1) umma_commit(qempty(qb));
+          }
+          __syncwarp();
+        } else {
+          // O^T += V_J^T P_J once V_J has landed and the softmax has written P_J
+          const int vs = J % kVStages;
+          const int pb = J & 1;
+          bool k = waitb(vfull(vs), (J / kVStages) & 1) && waitb(pfull(pb), (J >> 1) & 1);
+          if (k && t == 0 && I >= 3) k = waitb(ofree(ob), ((I / 3) - 1) & 1);
+          if (!__all_sync(0xffffffffu, k)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if (lane == 0) {
+            const uint64_t da0 = umma_desc_sw128(sV + vs * kTileBytes, kStrip, 1024);
+            const uint64_t db0 = umma_desc_mn_t<NC>(sP, 8 * NC * 2);
+#pragma unroll
+            for (int kk = 0; kk < kTok / 16; ++kk) {   // 16 tokens per k-step
+              const uint64_t da = da0 + static_cast<uint64_t>((kk * 2048) >> 4);
+              const uint64_t db = db0 + static_cast<uint64_t>((kk * 16 * NC * 2) >> 4);
+              umma_f16(tO + ob * NC, da, db, id_o, (t == 0 && kk == 0) ? 0u : 1u);
+            }
+            umma_commit(pfree(pb));
+            umma_commit(vempty(vs));
+            if (t == g.ntiles - 1) umma_commit(ofull(ob));
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if (pend && !issue_pv()) {
-          ok = false;
-          break;
-        }
-        pend = true;
-        pJ = J;
-        pI = I;
-        pfirst = t == 0;
-        plast = t == g.ntiles - 1;
-        ++J;
       }
       ++I;
     }
-    if (ok && pend && !issue_pv()) ok = false;
     if (!ok) abort_sh = 1;
-    // every MMA issued has completed before the CTA tears down
+    // every MMA issued has completed before the CTA tears down (one arrival per issuer)
     if (lane == 0) umma_commit(final_bar);
     mbar_wait_bounded(final_bar, 0, 100000000ull);
   } else if (warp < 4) {
@@ -557,10 +592,20 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const uint32_t prow_off = (t >> 3) * (8 * NC * 2) + (t & 7) * (NC * 2);
     const int pswz = NC == 32 ? (t >> 1) & 3 : (t >> 2) & 1;
     Walk w = make_walk();
-    Segment g;
+    Walk wn = make_walk();   // one segment ahead: its first block id is fetched early
+    Segment g, gn;
+    bool have_n = next_segment(a, wn, ntot, geff, gn, ctx_sh, walk_i[0]);
+    auto first_id = [&](const Segment& sg) {
+      const int tk = sg.j0 * kTok + t;
+      return tk < sg.ctx ? __ldg(a.block_tables + static_cast<size_t>(sg.s) * a.max_blocks_per_seq + tk / kBlock) : 0;
+    };
+    int id_seg = have_n ? first_id(gn) : 0;
     int J = 0, I = 0, nraise = 0;
     bool ok = true;
-    while (next_segment(a, w, ntot, geff, g)) {
+    while (next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+      int id_next = id_seg;
+      have_n = have_n && next_segment(a, wn, ntot, geff, gn, ctx_sh, walk_i[0]);
+      if (have_n) id_seg = first_id(gn);
       // per column: the running sum of this row's weights, and the CTA's reference in
       // registers (-inf while there is none; shared memory holds the copy a raise updates)
       float l_part[CU], mu_r[CU];
@@ -575,8 +620,6 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       // block id of this thread's row, one tile ahead (a row past the context or in a
       // block outside the pool is masked)
       const int32_t* table = a.block_tables + static_cast<size_t>(g.s) * a.max_blocks_per_seq;
-      const int tok0 = g.j0 * kTok + t;
-      int id_next = tok0 < g.ctx ? __ldg(table + tok0 / kBlock) : 0;
       for (int tt = 0; tt < g.ntiles; ++tt) {
         const int jt = g.j0 + tt;
         const int tok = jt * kTok + t;
@@ -631,7 +674,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
               abort_sh = 1;
             } else {
               tc_fence_after_sync();
-              const uint32_t to = tO + (I & 1) * NC + lane_base;
+              const uint32_t to = tO + (I % 3) * NC + lane_base;
 #pragma unroll
               for (int h = 0; h < (CU + 15) / 16; ++h) {
                 float o[16];
@@ -653,8 +696,9 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           fresh = false;
         }
         // P = 2^(x - reference) and the column sums; the row of P into shared memory
+        // P has one buffer: the previous tile's product must have read it
         const int pb = J & 1;
-        bool k3 = J < 2 || waitb(pfree(pb), ((J >> 1) - 1) & 1);
+        bool k3 = J < 1 || waitb(pfree((J - 1) & 1), ((J - 1) >> 1) & 1);
         if (!__all_sync(0xffffffffu, k3)) abort_sh = 1;
         uint32_t pk[CU / 2];
 #pragma unroll
@@ -666,7 +710,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           l_part[c + 1] += p1;
           pk[c / 2] = Mma<T>::pack(p0, p1);
         }
-        const uint32_t prow = sP + pb * L::PBYTES + prow_off;
+        const uint32_t prow = sP + prow_off;
 #pragma unroll
         for (int j = 0; j < CU / 8; ++j)
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((j ^ pswz) << 4)), "r"(pk[4 * j]),
@@ -703,8 +747,8 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       }
       // the segment's column sums and references for the epilogue
       const float lsum = warp_columns<CU, false>(l_part, lane);
-      const int sbuf = I & 1;
-      bool k4 = I < 2 || waiti(stfree(sbuf), ((I >> 1) - 1) & 1);
+      const int sbuf = I % 3;
+      bool k4 = I < 3 || waiti(stfree(sbuf), ((I / 3) - 1) & 1);
       if (!__all_sync(0xffffffffu, k4)) abort_sh = 1;
       if (lane < CU) st_l[sbuf][warp][lane] = lsum;
       if (warp == 0 && lane < CU) st_m[sbuf][lane] = fresh ? -INFINITY : mu_sh[nraise & 1][lane];
@@ -728,77 +772,72 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         out[query_row(a, s, kvh, G, rem / D) * D + rem % D] = Elem<T>::from_f(0.f);
       }
     }
-    auto load_q = [&](const Segment& sg, int qb) {
-      const uint32_t qbase = sQ + qb * L::QBYTES;
-      const T* qg = static_cast<const T*>(a.q);
-      for (int idx = d; idx < NC * 16; idx += 128) {
-        const int c = idx >> 4;
-        const int cc = idx & 15;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < NQ) v = __ldg(reinterpret_cast<const uint4*>(qg + query_row(a, sg.s, sg.kvh, G, c) * D) + cc);
-        const uint32_t dst = qbase + (cc >> 3) * L::QSTRIP + c * 128 + (((cc & 7) ^ (c & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qfull(qb));
-    };
-    Walk wq = make_walk();
     Walk w = make_walk();
-    Segment g, gq;
+    Segment g;
     int I = 0;
     bool ok = true;
-    bool have_next = next_segment(a, wq, ntot, geff, gq);
-    if (have_next) load_q(gq, 0);
-    while (next_segment(a, w, ntot, geff, g)) {
-      // q of the next segment, once the segment before this one no longer reads its buffer
-      have_next = have_next && next_segment(a, wq, ntot, geff, gq);
-      if (have_next) {
-        const int nb = (I + 1) & 1;
-        bool k = I + 1 < 2 || waiti(qempty(nb), (((I + 1) >> 1) - 1) & 1);
-        if (__all_sync(0xffffffffu, k))
-          load_q(gq, nb);
-        else
-          abort_sh = 1;
-      }
-      const int ob = I & 1;
-      bool k = waiti(ofull(ob), (I >> 1) & 1);
-      k = __all_sync(0xffffffffu, k) && waiti(stfull(ob), (I >> 1) & 1);
+    const int Hq = a.num_q_heads;
+    while (next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+      const int ob = I % 3;
+      bool k = waiti(ofull(ob), (I / 3) & 1);
+      k = __all_sync(0xffffffffu, k) && waiti(stfull(ob), (I / 3) & 1);
       k = __all_sync(0xffffffffu, k);
       if (cta_any(2, !k)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      float o[NC];
-      if constexpr (NC == 32)
-        tmem_ld32(tO + ob * NC + lane_base, o);
-      else
-        tmem_ld16(tO + ob * NC + lane_base, o);
+      float o[CU];
+      load_cols<CU>(tO + ob * NC + lane_base, o);
       tc_fence_before_sync();
+      // this thread's normalised output of every column; the statistics are copied out
+      // so both buffers return to their producers at once
+      float my_lse = -INFINITY;   // log2-sum-exp2 of column d (thread d stores it)
+#pragma unroll
+      for (int c = 0; c < CU; ++c) {
+        const float l = (st_l[ob][0][c] + st_l[ob][1][c]) + (st_l[ob][2][c] + st_l[ob][3][c]);
+        o[c] = l > 0.f ? o[c] / l : 0.f;
+        if (c == d && l > 0.f) my_lse = st_m[ob][c] + log2f(l);
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(ofree(ob));
-      auto col_sum = [&](int c) {
-        return (st_l[ob][0][c] + st_l[ob][1][c]) + (st_l[ob][2][c] + st_l[ob][3][c]);
-      };
+      if (lane == 0) {
+        mbar_arrive(ofree(ob));
+        mbar_arrive(stfree(ob));
+      }
+      // output row of column c = i G + h: (s q_len + i) Hq + kvh G + h, walked without division
+      const size_t row0 = static_cast<size_t>(g.s) * a.q_len * Hq + static_cast<size_t>(g.kvh) * G;
       if (g.n_parts == 1) {
         T* out = static_cast<T*>(a.out);
+        size_t row = row0;
+        int h = 0;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          if (c < NQ) {
-            const float l = col_sum(c);
-            out[query_row(a, g.s, g.kvh, G, c) * D + d] = Elem<T>::from_f(l > 0.f ? o[c] / l : 0.f);
+        for (int c = 0; c < CU; ++c) {
+          if (c < NQ) out[row * D + d] = Elem<T>::from_f(o[c]);
+          if (++h == G) {
+            h = 0;
+            row += Hq - G + 1;
+          } else {
+            ++row;
           }
         }
       } else {
+        const int ms = a.max_splits;
+        {
+          size_t row = row0;
+          int h = 0;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          if (c < NQ) {
-            const float l = col_sum(c);
-            const size_t row = query_row(a, g.s, g.kvh, G, c) * a.max_splits + g.part;
-            a.ws_o[row * D + d] = l > 0.f ? o[c] / l : 0.f;
-            if (d == c) a.ws_lse[row] = l > 0.f ? st_m[ob][c] + log2f(l) : -INFINITY;
+          for (int c = 0; c < CU; ++c) {
+            if (c < NQ) {
+              const size_t r = row * ms + g.part;
+              a.ws_o[r * D + d] = o[c];
+              if (d == c) a.ws_lse[r] = my_lse;
+            }
+            if (++h == G) {
+              h = 0;
+              row += Hq - G + 1;
+            } else {
+              ++row;
+            }
           }
         }
         // the CTA that stores the last segment of (s, kvh) merges them all
@@ -811,13 +850,48 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         }
         group_sync(2);
         if (last_sh) {
-          merge_split_partials<T, D>(a, g.s, g.kvh, G, g.n_parts, d, 128);
+          // log-sum-exp over the partials, 8 columns at a time, one partial at a time with
+          // a running maximum; each pass issues its 16 loads together
+          T* out = static_cast<T*>(a.out);
+#pragma unroll
+          for (int cg = 0; cg < CU; cg += 8) {
+            size_t rows[8];
+            float M[8], Ls[8], Os[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int c = cg + k;
+              rows[k] = query_row(a, g.s, g.kvh, G, c < NQ ? c : 0);
+              M[k] = -INFINITY;
+              Ls[k] = 0.f;
+              Os[k] = 0.f;
+            }
+            for (int pp = 0; pp < g.n_parts; ++pp) {
+              float lp[8], op[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const size_t r = rows[k] * ms + pp;
+                lp[k] = cg + k < NQ ? __ldcg(a.ws_lse + r) : -INFINITY;
+                op[k] = cg + k < NQ ? __ldcg(a.ws_o + r * D + d) : 0.f;
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (lp[k] == -INFINITY) continue;   // an empty partial weighs nothing
+                const float mn = fmaxf(M[k], lp[k]);
+                const float r0 = exp2f(M[k] - mn);  // 0 while M is still -inf
+                const float wgt = exp2f(lp[k] - mn);
+                Ls[k] = Ls[k] * r0 + wgt;
+                Os[k] = Os[k] * r0 + wgt * op[k];
+                M[k] = mn;
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (cg + k < NQ) out[rows[k] * D + d] = Elem<T>::from_f(Ls[k] > 0.f ? Os[k] / Ls[k] : 0.f);
+          }
           if (d == 0) *counter = 0;   // zero again for the next call on this workspace
         }
         group_sync(2);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(stfree(ob));
       ++I;
     }
     if (!ok) abort_sh = 1;
