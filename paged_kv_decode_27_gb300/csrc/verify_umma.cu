@@ -14,11 +14,12 @@
 //
 // Work split (stream-K): the (sequence, KV head, 128-token tile) triples, in
 // sequence-major order, are cut into one contiguous range per CTA of equal
-// length (at least `part_blocks / 8` tiles), so every SM streams the same
-// number of tiles whatever the context lengths.  A range covers whole or
-// partial (sequence, KV head) runs, "segments"; a (sequence, KV head) split
-// over several CTAs leaves one normalised partial per segment and the CTA that
-// finishes its segment last merges them by log-sum-exp (decode_merge.cuh).
+// cost (at least `part_blocks / 8` tiles), so every SM finishes at the same
+// time whatever the context lengths; a run's cost counts its tiles and the
+// fixed cost of starting it.  A range covers whole or partial (sequence, KV
+// head) runs, "segments"; a (sequence, KV head) split over several CTAs leaves
+// one normalised partial per segment and the CTA that finishes its segment
+// last merges them by log-sum-exp.
 //
 // One CTA per SM, twelve warps with fixed roles:
 //   warps 0-3  softmax: thread t owns token row t of S^T (tensor memory lane
@@ -195,17 +196,30 @@ struct Segment {
   int n_parts, part;        // segments of (s, kvh) over all CTAs, and this one's index
 };
 
+// The split balances cost, not tiles: a (sequence, KV head) run of nt tiles
+// weighs nt * kUnitsTile + kUnitsSeg units (a tile, plus the fixed cost of a
+// segment: its first scores raise every reference, its statistics and outputs
+// are written once).  Tile j of a run at unit b sits at unit b + kUnitsTile * j
+// and belongs to the CTA whose range of units holds that point; ranges are at
+// least kUnitsTile long, so every CTA between a run's first and last owner holds
+// one of its tiles.
+constexpr int kUnitsTile = 4;
+constexpr int kUnitsSeg = 6;
+
 struct Walk {
   int s, kvh, j, ctx, nt;
-  long long base;           // global index of tile (s, 0, 0)
-  long long left;           // tiles of this CTA not yet visited
+  long long ibase;          // unit of the current run's first tile
+  long long x1;             // end of this CTA's range of units
 };
 
-__device__ __forceinline__ long long owner_of(long long x, long long T, int geff) {
-  return ((x + 1) * geff - 1) / T;
+__device__ __forceinline__ long long owner_of(long long x, long long V, int geff) {
+  return ((x + 1) * geff - 1) / V;
 }
 
 __device__ __forceinline__ int tiles_of(int ctx) { return (ctx + kTok - 1) / kTok; }
+__device__ __forceinline__ long long run_units(int nt) {
+  return nt > 0 ? static_cast<long long>(kUnitsTile) * nt + kUnitsSeg : 0;
+}
 
 // Contexts of the CTA's first kCtxCache sequences, cached in shared memory: every
 // role walks the same sequences, and a global load per new sequence would stall it.
@@ -216,15 +230,14 @@ __device__ __forceinline__ int walk_context(const DecodeArgs& a, const int* cach
 }
 
 // Next segment of the walk; false when the CTA's range is done.
-__device__ __forceinline__ bool next_segment(const DecodeArgs& a, Walk& w, long long T, int geff, Segment& g,
+__device__ __forceinline__ bool next_segment(const DecodeArgs& a, Walk& w, long long V, int geff, Segment& g,
                                              const int* cache, int s0) {
-  if (w.left <= 0) return false;
-  while (w.nt == 0 || w.j >= w.nt) {   // the walk never rests on an empty or finished sequence
+  while (w.nt == 0 || w.j >= w.nt) {   // the walk never rests on an empty or finished run
     if (w.nt > 0 && w.j >= w.nt) {
       w.j = 0;
+      w.ibase += run_units(w.nt);
       if (++w.kvh < a.num_kv_heads) continue;
     }
-    w.base += static_cast<long long>(w.nt) * a.num_kv_heads;
     w.kvh = 0;
     w.j = 0;
     ++w.s;
@@ -232,19 +245,21 @@ __device__ __forceinline__ bool next_segment(const DecodeArgs& a, Walk& w, long 
     w.ctx = walk_context(a, cache, s0, w.s);
     w.nt = tiles_of(w.ctx);
   }
+  const long long r = w.x1 - w.ibase;   // this CTA's tiles of the run: kUnitsTile * j < r
+  if (r <= 0) return false;
+  const int jend = static_cast<int>(min(static_cast<long long>(w.nt), (r + kUnitsTile - 1) / kUnitsTile));
+  if (jend <= w.j) return false;
   g.s = w.s;
   g.kvh = w.kvh;
   g.j0 = w.j;
   g.ctx = w.ctx;
   g.nt = w.nt;
-  g.ntiles = static_cast<int>(min(static_cast<long long>(w.nt - w.j), w.left));
-  const long long first = w.base + static_cast<long long>(w.kvh) * w.nt;
-  const long long c0 = owner_of(first, T, geff);
-  const long long c1 = owner_of(first + w.nt - 1, T, geff);
+  g.ntiles = jend - w.j;
+  const long long c0 = owner_of(w.ibase, V, geff);
+  const long long c1 = owner_of(w.ibase + static_cast<long long>(kUnitsTile) * (w.nt - 1), V, geff);
   g.n_parts = static_cast<int>(c1 - c0 + 1);
   g.part = static_cast<int>(blockIdx.x - c0);
-  w.j += g.ntiles;
-  w.left -= g.ntiles;
+  w.j = jend;
   return true;
 }
 
@@ -267,7 +282,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   __shared__ float mu_sh[2][NC];
   __shared__ float st_l[3][4][NC];             // per segment: column sums of each softmax warp
   __shared__ float st_m[3][NC];                // per segment: column references
-  __shared__ long long walk_sh[3];             // start base, tiles left, total tiles
+  __shared__ long long walk_sh[3];             // first run's unit, end of the range, total units
   __shared__ int walk_i[4];                    // s, kvh, j, geff
   __shared__ int ctx_sh[kCtxCache];            // contexts of sequences walk_i[0] ...
   __shared__ uint32_t tmem_base_sh;
@@ -334,48 +349,47 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   }
   // ---- the CTA's range of the global tile order (warp 8) ----------------------
   if (warp == 8) {
-    long long tsum = 0;   // tiles of one KV head over all sequences
+    long long usum = 0;   // units of one KV head over all sequences
     for (int s0 = 0; s0 < a.num_seqs; s0 += 32) {
       const int s = s0 + lane;
-      const int nt = s < a.num_seqs ? tiles_of(checked_context(a, s, blockIdx.x == 0)) : 0;
-      int v = nt;
+      long long v = s < a.num_seqs ? run_units(tiles_of(checked_context(a, s, blockIdx.x == 0))) : 0;
 #pragma unroll
       for (int m = 1; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-      tsum += v;
+      usum += v;
     }
-    const long long ntot = tsum * H;
+    const long long vtot = usum * H;
     const long long lmin = a.part_blocks >= kTileBlocks ? a.part_blocks / kTileBlocks : 1;
-    long long ge = ntot / lmin;
+    long long ge = vtot / (lmin * kUnitsTile);
     ge = ge < 1 ? 1 : ge;
     const int geff = static_cast<int>(ge < gridDim.x ? ge : gridDim.x);
     const long long c = blockIdx.x;
-    const long long start = c < geff ? c * ntot / geff : ntot;
-    const long long end = c < geff ? (c + 1) * ntot / geff : ntot;
-    // locate `start`: sequence s with H * pre(s) <= start < H * pre(s + 1)
-    long long pre = 0;   // H * tiles of the sequences before the current chunk
+    const long long x0 = c < geff ? c * vtot / geff : vtot;
+    const long long x1 = c < geff ? (c + 1) * vtot / geff : vtot;
+    // locate x0: sequence s whose H runs span [pre, pre + H * units(s)) around it
+    long long pre = 0;
     int fs = a.num_seqs, fkvh = 0, fj = 0;
-    long long fbase = ntot;
+    long long fbase = vtot;
     for (int s0 = 0; s0 < a.num_seqs && fs == a.num_seqs; s0 += 32) {
       const int s = s0 + lane;
-      const int nt = s < a.num_seqs ? tiles_of(checked_context(a, s, false)) : 0;
-      long long incl = static_cast<long long>(nt) * H;
+      const long long u = s < a.num_seqs ? run_units(tiles_of(checked_context(a, s, false))) : 0;
+      long long incl = u * H;
 #pragma unroll
       for (int m = 1; m < 32; m <<= 1) {
         const long long o = __shfl_up_sync(0xffffffffu, incl, m);
         if (lane >= m) incl += o;
       }
-      const long long excl = incl - static_cast<long long>(nt) * H;
-      const bool hit = s < a.num_seqs && nt > 0 && pre + excl <= start && start < pre + incl;
+      const long long excl = incl - u * H;
+      const bool hit = s < a.num_seqs && u > 0 && pre + excl <= x0 && x0 < pre + incl;
       const unsigned hm = __ballot_sync(0xffffffffu, hit);
       if (hm) {
         const int src = __ffs(hm) - 1;
         const long long b = __shfl_sync(0xffffffffu, pre + excl, src);
-        const int nts = __shfl_sync(0xffffffffu, nt, src);
+        const long long us = __shfl_sync(0xffffffffu, u, src);
         fs = s0 + src;
-        fbase = b;
-        const long long off = start - b;
-        fkvh = static_cast<int>(off / nts);
-        fj = static_cast<int>(off % nts);
+        const long long off = x0 - b;
+        fkvh = static_cast<int>(off / us);
+        fbase = b + fkvh * us;
+        fj = static_cast<int>((off - fkvh * us + kUnitsTile - 1) / kUnitsTile);   // may pass the run's end
       }
       pre += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -383,8 +397,8 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       ctx_sh[k] = fs + k < a.num_seqs ? checked_context(a, fs + k, false) : 0;
     if (lane == 0) {
       walk_sh[0] = fbase;
-      walk_sh[1] = end - start;
-      walk_sh[2] = ntot;
+      walk_sh[1] = x1;
+      walk_sh[2] = vtot;
       walk_i[0] = fs;
       walk_i[1] = fkvh;
       walk_i[2] = fj;
@@ -399,15 +413,15 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const long long ntot = walk_sh[2];
+  const long long vtot = walk_sh[2];
   const int geff = walk_i[3];
   auto make_walk = [&]() {
     Walk w;
     w.s = walk_i[0];
     w.kvh = walk_i[1];
     w.j = walk_i[2];
-    w.base = walk_sh[0];
-    w.left = walk_sh[1];
+    w.ibase = walk_sh[0];
+    w.x1 = walk_sh[1];
     w.ctx = w.s < a.num_seqs ? ctx_sh[0] : 0;
     w.nt = tiles_of(w.ctx);
     return w;
@@ -438,7 +452,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     Segment g;
     int J = 0, I = 0;
     bool ok = true;
-    while (ok && next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+    while (ok && next_segment(a, w, vtot, geff, g, ctx_sh, walk_i[0])) {
       if (isk) {
         // the segment's q, K-major and 128-byte swizzled, once segment I - 2's scores are done
         const int qb = I & 1;
@@ -515,7 +529,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     Segment g;
     int J = 0, I = 0;
     bool ok = true;
-    while (ok && next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+    while (ok && next_segment(a, w, vtot, geff, g, ctx_sh, walk_i[0])) {
       const int qb = I & 1;
       const int ob = I % 3;
       if (is_s) {
@@ -594,7 +608,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     Walk w = make_walk();
     Walk wn = make_walk();   // one segment ahead: its first block id is fetched early
     Segment g, gn;
-    bool have_n = next_segment(a, wn, ntot, geff, gn, ctx_sh, walk_i[0]);
+    bool have_n = next_segment(a, wn, vtot, geff, gn, ctx_sh, walk_i[0]);
     auto first_id = [&](const Segment& sg) {
       const int tk = sg.j0 * kTok + t;
       return tk < sg.ctx ? __ldg(a.block_tables + static_cast<size_t>(sg.s) * a.max_blocks_per_seq + tk / kBlock) : 0;
@@ -602,9 +616,9 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     int id_seg = have_n ? first_id(gn) : 0;
     int J = 0, I = 0, nraise = 0;
     bool ok = true;
-    while (next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+    while (next_segment(a, w, vtot, geff, g, ctx_sh, walk_i[0])) {
       int id_next = id_seg;
-      have_n = have_n && next_segment(a, wn, ntot, geff, gn, ctx_sh, walk_i[0]);
+      have_n = have_n && next_segment(a, wn, vtot, geff, gn, ctx_sh, walk_i[0]);
       if (have_n) id_seg = first_id(gn);
       // per column: the running sum of this row's weights, and the CTA's reference in
       // registers (-inf while there is none; shared memory holds the copy a raise updates)
@@ -777,7 +791,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     int I = 0;
     bool ok = true;
     const int Hq = a.num_q_heads;
-    while (next_segment(a, w, ntot, geff, g, ctx_sh, walk_i[0])) {
+    while (next_segment(a, w, vtot, geff, g, ctx_sh, walk_i[0])) {
       const int ob = I % 3;
       bool k = waiti(ofull(ob), (I / 3) & 1);
       k = __all_sync(0xffffffffu, k) && waiti(stfull(ob), (I / 3) & 1);
@@ -796,7 +810,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 #pragma unroll
       for (int c = 0; c < CU; ++c) {
         const float l = (st_l[ob][0][c] + st_l[ob][1][c]) + (st_l[ob][2][c] + st_l[ob][3][c]);
-        o[c] = l > 0.f ? o[c] / l : 0.f;
+        o[c] *= l > 0.f ? __frcp_rn(l) : 0.f;
         if (c == d && l > 0.f) my_lse = st_m[ob][c] + log2f(l);
       }
       __syncwarp();
@@ -877,8 +891,8 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
               for (int k = 0; k < 8; ++k) {
                 if (lp[k] == -INFINITY) continue;   // an empty partial weighs nothing
                 const float mn = fmaxf(M[k], lp[k]);
-                const float r0 = exp2f(M[k] - mn);  // 0 while M is still -inf
-                const float wgt = exp2f(lp[k] - mn);
+                const float r0 = fast_exp2(M[k] - mn);  // 0 while M is still -inf
+                const float wgt = fast_exp2(lp[k] - mn);
                 Ls[k] = Ls[k] * r0 + wgt;
                 Os[k] = Os[k] * r0 + wgt * op[k];
                 M[k] = mn;
@@ -886,7 +900,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              if (cg + k < NQ) out[rows[k] * D + d] = Elem<T>::from_f(Ls[k] > 0.f ? Os[k] / Ls[k] : 0.f);
+              if (cg + k < NQ) out[rows[k] * D + d] = Elem<T>::from_f(Ls[k] > 0.f ? Os[k] * __frcp_rn(Ls[k]) : 0.f);
           }
           if (d == 0) *counter = 0;   // zero again for the next call on this workspace
         }
@@ -936,7 +950,7 @@ cudaError_t launch_vu_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUte
 int verify_umma_slots(int max_context_len, int part_blocks) {
   const int lmin = part_blocks >= kTileBlocks ? part_blocks / kTileBlocks : 1;
   const int nt = (max_context_len + kTok - 1) / kTok;
-  return (nt + lmin - 1) / lmin + 1;
+  return (nt + lmin - 1) / lmin + 2;
 }
 
 cudaError_t launch_verify_umma(const DecodeArgs& a, int dtype, const CUtensorMap& kmap, const CUtensorMap& vmap,

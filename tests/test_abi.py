@@ -190,9 +190,10 @@ def test_verify_validates_on_the_host(lib):
     assert lib.pa_verify_workspace_size(64, 1, 32, 8224, 0, ctypes.byref(d)) == \
         lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(d))
     # head dim 128, q_len > 1: the tensor-core kernel keeps one partial per stream-K
-    # segment; with 1024-token partitions a segment spans >= 8 tiles of 128 tokens, so
-    # a context of 8224 tokens (65 tiles) meets at most ceil(65 / 8) + 1 = 10 segments
-    rows = 64 * 5 * 32 * 10
+    # segment; with 1024-token partitions a CTA's range costs at least 8 tiles, so a
+    # context of 8224 tokens (65 tiles, plus its start-up cost) meets at most
+    # ceil(65 / 8) + 2 = 11 ranges
+    rows = 64 * 5 * 32 * 11
     assert lib.pa_verify_workspace_size(64, 5, 32, 8224, 0, ctypes.byref(d)) == \
         ((256 * 1024 + rows * 128 * 4 + 255) // 256) * 256 + rows * 4
     # head dim 64 stays on the mma.sync kernel: one partial per 1024-token partition
