@@ -204,7 +204,7 @@ struct Segment {
 // least kUnitsTile long, so every CTA between a run's first and last owner holds
 // one of its tiles.
 constexpr int kUnitsTile = 4;
-constexpr int kUnitsSeg = 6;
+constexpr int kUnitsSeg = 16;
 
 struct Walk {
   int s, kvh, j, ctx, nt;
