@@ -206,7 +206,10 @@ PA_API int pa_decode_step(void* out, const void* q, void* k_pool, void* v_pool, 
  * attends keys 0..p (causal), exactly as a prompt pass over a cached prefix
  * would; q_len = 1 is pa_decode_attention.  The K/V blocks are read once for
  * all q_len x G query rows of a KV head, and long contexts are split into
- * partitions merged by log-sum-exp as in pa_decode_attention.
+ * pieces merged by log-sum-exp as in pa_decode_attention.  At head dim 128 the
+ * pieces are the stream-K ranges of a persistent launch (one CTA per SM, each
+ * range at least partition_size tokens of work, 1024 when partition_size is
+ * 0); at head dim 64 they are partitions of partition_size tokens.
  *
  *   out, q        : [num_seqs][q_len][num_q_heads][D], bf16 or fp16 pools
  *   context_lens  : int32 [num_seqs], each >= q_len (rows whose position is
