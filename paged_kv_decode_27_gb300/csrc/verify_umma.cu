@@ -31,7 +31,7 @@
 //   warps 4-7  epilogue: thread d owns head-dim row d of O^T.  It normalises
 //              and stores each finished segment and runs the split-K merge;
 //              none of this holds up the tiles of the next segments.
-//   warps 8/10 TMA producers of K tiles and V tiles (3 stages each) of
+//   warps 8/10 TMA producers of K tiles (2 stages) and V tiles (3 stages) of
 //              8 pool blocks through the block table; blocks past the context
 //              or with an id outside the pool are read as zeros.  The K warp
 //              also stages each segment's q, ahead of its first K tile.
@@ -60,7 +60,7 @@ constexpr int kTileBlocks = kTok / kBlock;     // 8 pool blocks
 constexpr int kDim = 128;                      // head dim (MMA M of O^T)
 constexpr int kStrip = kTok * 128;             // one 64-column strip of a K or V tile
 constexpr int kTileBytes = 2 * kStrip;         // 32 KB
-constexpr int kKStages = 3;
+constexpr int kKStages = 2;
 constexpr int kVStages = 3;
 constexpr int kUThreads = 384;
 constexpr float kLazyU = 8.f;                  // log2 headroom of the softmax reference
@@ -69,12 +69,12 @@ template <int NC>
 struct VLayout {
   static constexpr int QSTRIP = NC * 128;      // one 64-column strip of q (NC rows)
   static constexpr int QBYTES = 2 * QSTRIP;
-  static constexpr int PBYTES = kTok * NC * 2; // P: 128 token rows of NC columns (one buffer)
+  static constexpr int PBYTES = kTok * NC * 2; // P: 128 token rows of NC columns (two buffers)
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + kKStages * kTileBytes;
   static constexpr int Q_OFF = V_OFF + kVStages * kTileBytes;
   static constexpr int P_OFF = Q_OFF + 2 * QBYTES;
-  static constexpr int SMEM = P_OFF + PBYTES;
+  static constexpr int SMEM = P_OFF + 2 * PBYTES;
   static constexpr uint32_t TMEM_COLS = NC == 32 ? 256 : 128;   // S^T x2, O^T x3 (a power of two)
 };
 
@@ -578,7 +578,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           tc_fence_after_sync();
           if (lane == 0) {
             const uint64_t da0 = umma_desc_sw128(sV + vs * kTileBytes, kStrip, 1024);
-            const uint64_t db0 = umma_desc_mn_t<NC>(sP, 8 * NC * 2);
+            const uint64_t db0 = umma_desc_mn_t<NC>(sP + pb * L::PBYTES, 8 * NC * 2);
 #pragma unroll
             for (int kk = 0; kk < kTok / 16; ++kk) {   // 16 tokens per k-step
               const uint64_t da = da0 + static_cast<uint64_t>((kk * 2048) >> 4);
@@ -710,9 +710,9 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           fresh = false;
         }
         // P = 2^(x - reference) and the column sums; the row of P into shared memory
-        // P has one buffer: the previous tile's product must have read it
+        // P alternates between two buffers: the product of tile J - 2 must have read this one
         const int pb = J & 1;
-        bool k3 = J < 1 || waitb(pfree((J - 1) & 1), ((J - 1) >> 1) & 1);
+        bool k3 = J < 2 || waitb(pfree(pb), ((J >> 1) - 1) & 1);
         if (!__all_sync(0xffffffffu, k3)) abort_sh = 1;
         uint32_t pk[CU / 2];
 #pragma unroll
@@ -724,7 +724,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           l_part[c + 1] += p1;
           pk[c / 2] = Mma<T>::pack(p0, p1);
         }
-        const uint32_t prow = sP + prow_off;
+        const uint32_t prow = sP + pb * L::PBYTES + prow_off;
 #pragma unroll
         for (int j = 0; j < CU / 8; ++j)
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((j ^ pswz) << 4)), "r"(pk[4 * j]),

@@ -42,6 +42,7 @@ def _ref(wl, q, ctx, seqs=None):
     (32, 8, 5, 128, torch.bfloat16),    # G 4 x 5 positions: 20 columns (three 8-column tiles)
     (32, 4, 4, 128, torch.bfloat16),    # G 8 x 4: 32 columns (four tiles)
     (8, 8, 5, 128, torch.float16),      # G 1 x 5: one tile
+    (16, 8, 5, 128, torch.bfloat16),    # G 2 x 5: 10 columns (the 16-column tensor-core kernel)
     (16, 8, 5, 64, torch.bfloat16),     # G 2 x 5: two tiles, D 64
     (12, 4, 8, 64, torch.float16),      # G 3 x 8: 24 columns, D 64
     (32, 8, 1, 128, torch.bfloat16),    # q_len 1 is decode
@@ -131,3 +132,51 @@ def test_verify_llama3_8b_full_size_sampled():
     ref = _ref(wl, q, ctx, seqs=pick)
     assert_close_to_ref(out[pick], ref[pick], wl.dtype, "verify llama3-8b")
     assert pa.pa_device_status() == 0
+
+
+def test_verify_d128_empty_and_short_contexts():
+    """Head dim 128 (the tensor-core kernel): a context of 0 owns no tile and
+    its rows are zero; a context shorter than q_len zeroes the leading rows."""
+    ctx_l = [3, 0, 9, 0, 130, 1]
+    wl = W.small_random(102, len(ctx_l), 0, 32, 8, 128, torch.bfloat16, ctx=ctx_l)
+    ctx = torch.tensor(ctx_l, dtype=torch.int32)
+    q = wl.verify_queries(0, 5)
+    out = _verify(wl, q, ctx)
+    assert int(out[1].count_nonzero()) == 0 and int(out[3].count_nonzero()) == 0
+    assert int(out[0, :2].count_nonzero()) == 0 and int(out[5, :4].count_nonzero()) == 0
+    assert_close_to_ref(out, _ref(wl, q, ctx), wl.dtype, "empty and short contexts, D 128")
+    assert pa.pa_device_status() == 0
+
+
+@pytest.mark.parametrize("part", [0, 128, 1024])
+def test_verify_many_segments_per_cta(part):
+    """Ninety mostly short sequences: every CTA of the persistent launch walks
+    many (sequence, KV head) segments, long ones are split over several CTAs
+    and merged."""
+    g = torch.Generator().manual_seed(7)
+    ctx_l = [int(x) for x in torch.randint(1, 400, (88,), generator=g)] + [3000, 5000]
+    wl = W.small_random(103, len(ctx_l), 0, 32, 8, 128, torch.bfloat16, ctx=ctx_l)
+    ctx = torch.tensor(ctx_l, dtype=torch.int32).clamp(min=5)
+    q = wl.verify_queries(0, 5)
+    pick = list(range(0, 90, 7)) + [88, 89]
+    out = _verify(wl, q, ctx, part)
+    ref = _ref(wl, q, ctx, seqs=pick)
+    assert_close_to_ref(out[pick], ref[pick], wl.dtype, f"many segments part={part}")
+    assert pa.pa_device_status() == 0
+
+
+def test_verify_d128_bad_block_id_is_reported():
+    wl = W.small_random(104, 3, 0, 32, 8, 128, torch.bfloat16, ctx=[200, 300, 90])
+    ctx = torch.tensor([200, 300, 90], dtype=torch.int32)
+    bt = wl.decode_block_tables.clone()
+    bt[1, 3] = wl.num_blocks + 1000
+    bt[2, 0] = -7
+    q = wl.verify_queries(0, 5)
+    out = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    pa.pa_verify_attention(out, q.to(DEV), wl.k_pool.to(DEV), wl.v_pool.to(DEV), bt.to(DEV), ctx.to(DEV),
+                           wl.scale, max_context_len=300)
+    torch.cuda.synchronize()
+    assert pa.pa_device_status() & pa.PA_DEV_BAD_BLOCK_ID
+    # sequence 0 is untouched by the bad entries
+    ref = _ref(wl, q, ctx, seqs=[0])
+    assert_close_to_ref(out[:1], ref[:1], wl.dtype, "good row next to bad ones, D 128")
