@@ -279,7 +279,7 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   __shared__ __align__(8) uint64_t bars[37];
   __shared__ float red_sh[4][NC];              // column maxima of a raise, per softmax warp
   // The CTA's column references, alternating by raise (-inf while a column has none).
-  __shared__ float mu_sh[2][NC];
+  __shared__ __align__(16) float mu_sh[2][NC];
   __shared__ float st_l[3][4][NC];             // per segment: column sums of each softmax warp
   __shared__ float st_m[3][NC];                // per segment: column references
   __shared__ long long walk_sh[3];             // first run's unit, end of the range, total units
@@ -675,37 +675,39 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             mu_sh[nb_][lane] = fmaxf(fresh ? -INFINITY : mu_sh[ob_][lane], mx);
           }
           group_sync(1);
-          // 2^(old - new) per column (1 while it had no reference)
-          auto alpha = [&](int c) { return mu_r[c] != -INFINITY ? fast_exp2(mu_r[c] - mu_sh[nb_][c]) : 1.f; };
-          bool grew = false;
+          if (!fresh) {   // the first raise of a segment has nothing to rescale
+            // 2^(old - new) per column (1 while it had no reference)
+            auto alpha = [&](int c) { return mu_r[c] != -INFINITY ? fast_exp2(mu_r[c] - mu_sh[nb_][c]) : 1.f; };
+            bool grew = false;
 #pragma unroll
-          for (int c = 0; c < CU; ++c) grew |= alpha(c) != 1.f;
-          if (tt > 0 && grew) {
-            // rescale O^T (lane t = head-dim row t) once the previous tile's product is done
-            const int pj = J - 1;
-            bool k2 = waitb(pfree(pj & 1), (pj >> 1) & 1);
-            if (!__all_sync(0xffffffffu, k2)) {
-              abort_sh = 1;
-            } else {
-              tc_fence_after_sync();
-              const uint32_t to = tO + (I % 3) * NC + lane_base;
+            for (int c = 0; c < CU; ++c) grew |= alpha(c) != 1.f;
+            if (tt > 0 && grew) {
+              // rescale O^T (lane t = head-dim row t) once the previous tile's product is done
+              const int pj = J - 1;
+              bool k2 = waitb(pfree(pj & 1), (pj >> 1) & 1);
+              if (!__all_sync(0xffffffffu, k2)) {
+                abort_sh = 1;
+              } else {
+                tc_fence_after_sync();
+                const uint32_t to = tO + (I % 3) * NC + lane_base;
 #pragma unroll
-              for (int h = 0; h < (CU + 15) / 16; ++h) {
-                float o[16];
-                tmem_ld16(to + 16 * h, o);
-                uint32_t ob[16];
+                for (int h = 0; h < (CU + 15) / 16; ++h) {
+                  float o[16];
+                  tmem_ld16(to + 16 * h, o);
+                  uint32_t ob[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) ob[c] = __float_as_uint(16 * h + c < CU ? o[c] * alpha(16 * h + c) : o[c]);
-                tmem_st16_u(to + 16 * h, ob);
+                  for (int c = 0; c < 16; ++c)
+                    ob[c] = __float_as_uint(16 * h + c < CU ? o[c] * alpha(16 * h + c) : o[c]);
+                  tmem_st16_u(to + 16 * h, ob);
+                }
+                tmem_wait_st();
               }
-              tmem_wait_st();
             }
+#pragma unroll
+            for (int c = 0; c < CU; ++c) l_part[c] *= alpha(c);   // the sums follow
           }
 #pragma unroll
-          for (int c = 0; c < CU; ++c) {   // the sums follow; the new references into registers
-            l_part[c] *= alpha(c);
-            mu_r[c] = mu_sh[nb_][c];
-          }
+          for (int c = 0; c < CU; ++c) mu_r[c] = mu_sh[nb_][c];
           ++nraise;
           fresh = false;
         }
