@@ -33,8 +33,8 @@
 //              none of this holds up the tiles of the next segments.
 //   warps 8/10 TMA producers of K tiles (2 stages) and V tiles (3 stages) of
 //              8 pool blocks through the block table; blocks past the context
-//              or with an id outside the pool are read as zeros.  The K warp
-//              also stages each segment's q, ahead of its first K tile.
+//              or with an id outside the pool are read as zeros.  The V warp
+//              also stages each segment's q.
 //   warps 9/11 MMA issuers: S^T of tile j (warp 9) and O^T += V^T P of tile j
 //              (warp 11), so the scores of the next tile are computed while the
 //              softmax of this one runs.
@@ -453,8 +453,10 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     int J = 0, I = 0;
     bool ok = true;
     while (ok && next_segment(a, w, vtot, geff, g, ctx_sh, walk_i[0])) {
-      if (isk) {
-        // the segment's q, K-major and 128-byte swizzled, once segment I - 2's scores are done
+      if (!isk) {
+        // The segment's q, K-major and 128-byte swizzled, once segment I - 2's scores are done.
+        // The V warp stages it: its loads stall this warp for a memory latency, which the
+        // three V stages absorb, where the two K stages would run dry.
         const int qb = I & 1;
         ok = I < 2 || waiti(qempty(qb), ((I >> 1) - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
