@@ -283,6 +283,9 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // S_j = Q K_j^T once K_j has landed and PV_{j-1} (which read P from the
       // same columns) has completed
       ok = wait_all(k_full(st), (j / kStages) & 1) && (j < 1 || wait_all(pv_done(g), (j - 1) & 1));
+      // Tile B starts once tile A's first softmax is done, so that the two tiles run out of
+      // phase (one tile's MMAs during the other's softmax) instead of in step on every K tile.
+      if (ok && g == 1 && j == 0) ok = wait_all(p_full(0), 0);
       if (!ok) break;
       tc_fence_after_sync();
       if (lane == 0) {
