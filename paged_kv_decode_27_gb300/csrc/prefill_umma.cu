@@ -155,32 +155,41 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     fence_barrier_init();
     abort_sh = 0;
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
-    tmem_relinquish();
-  }
-  // Q tiles -> shared memory in the 128-byte-swizzled K-major layout
-  if (warp < 8) {
-    const int g = warp >> 2;
-    const int r = threadIdx.x & 127;
-    const int lr = (2 * pt + g) * kRows + r;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
-                                                      ((static_cast<size_t>(q0) + lr) * a.num_q_heads + hq) * D);
-    const uint32_t qbase = sQ + g * L::Q_BYTES;
-#pragma unroll
-    for (int cc = 0; cc < D / 8; ++cc) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (lr < n) v = src[cc];
-      const uint32_t dst = qbase + (cc >> 3) * L::HALF_Q + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
-    }
-    fence_proxy_async_smem();
-  }
-  tc_fence_before_sync();
+  // The barriers are ready: the producer starts streaming K/V tiles at once, while
+  // the other warps allocate tensor memory and stage Q (they meet on named barrier 1).
   __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = tmem_base_sh;
+  uint32_t tmem = 0;
+  if (warp != 8) {
+    if (warp == 0) {
+      tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+      tmem_relinquish();
+    }
+    // Q tiles -> shared memory in the 128-byte-swizzled K-major layout; every load of a
+    // row is in flight before the first store
+    if (warp < 8) {
+      const int g = warp >> 2;
+      const int r = threadIdx.x & 127;
+      const int lr = (2 * pt + g) * kRows + r;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
+                                                        ((static_cast<size_t>(q0) + lr) * a.num_q_heads + hq) * D);
+      const uint32_t qbase = sQ + g * L::Q_BYTES;
+      uint4 v[D / 8];
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) v[cc] = lr < n ? src[cc] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) {
+        const uint32_t dst = qbase + (cc >> 3) * L::HALF_Q + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v[cc].x), "r"(v[cc].y), "r"(v[cc].z),
+                     "r"(v[cc].w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");   // every warp but the producer
+    tc_fence_after_sync();
+    tmem = tmem_base_sh;
+  }
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
