@@ -6,8 +6,9 @@
 // Inference Server", Batched Scheduling & Speculative Decoding: K = 4): query
 // i of a sequence with context c sits at position c - q_len + i and sees keys
 // 0 .. c - q_len + i.  Per KV head the query columns are the G heads of the
-// group at every position (column x = i * G + h), NC = 16 or 32 of them with
-// the unused ones zero.  Every column of a (sequence, KV head) reads the same
+// group at every position (column x = i * G + h): NC = 16 or 32 MMA columns,
+// the unused ones zero, of which the softmax works on CU (the used ones rounded
+// up to 8).  Every column of a (sequence, KV head) reads the same
 // K/V, so the work is two thin matrix products per 128-token tile -- scores
 // S^T = K q^T (M = 128 tokens, N = NC, K = D) and O^T += V^T P (M = D,
 // N = NC, K = 128 tokens) -- with the softmax between them.
@@ -26,8 +27,9 @@
 //              t).  The softmax reference of each column is shared by the CTA
 //              and raised lazily (only when a score exceeds it by 2^8; a CTA-
 //              wide vote decides, a transpose reduction gives the column
-//              maxima).  P^T goes to shared memory in the K-major layout the
-//              second product reads; a raise rescales O^T in tensor memory.
+//              maxima).  Each thread writes its row of P (the second
+//              product's B operand, MN-major, 64- or 32-byte swizzle) to shared
+//              memory with 16-byte stores; a raise rescales O^T in tensor memory.
 //   warps 4-7  epilogue: thread d owns head-dim row d of O^T.  It normalises
 //              and stores each finished segment and runs the split-K merge;
 //              none of this holds up the tiles of the next segments.
@@ -38,8 +40,8 @@
 //   warps 9/11 MMA issuers: S^T of tile j (warp 9) and O^T += V^T P of tile j
 //              (warp 11), so the scores of the next tile are computed while the
 //              softmax of this one runs.
-// Tensor memory: two S^T buffers and two O^T buffers of NC columns (O^T
-// alternates by segment so the epilogue of one overlaps the next).
+// Tensor memory: two S^T buffers and three O^T buffers of NC columns (O^T
+// rotates by segment so the epilogues of the last two overlap the next).
 //
 // Stale pool rows past a sequence's last token are zeroed in shared memory
 // before the second product reads them (their weight is 0, and 0 * NaN is
