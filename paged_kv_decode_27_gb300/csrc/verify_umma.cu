@@ -659,7 +659,8 @@ verify_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         const bool tok_ok = tok < g.ctx && id >= 0 && id < a.num_blocks;
         const int cmin = tok <= lim0 ? 0 : G * (tok - lim0);   // first column this row may attend
         const bool whole = tok_ok && cmin == 0;                  // every column attends this row
-        // x = score in the log2 domain; a raise is due where x passes its reference + 2^3
+        // x = score in the log2 domain; a raise is due where x passes its reference by more
+        // than kLazyU (a factor of 2^8)
         bool need = false;
 #pragma unroll
         for (int c = 0; c < CU; ++c) {
