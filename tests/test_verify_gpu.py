@@ -43,6 +43,8 @@ def _ref(wl, q, ctx, seqs=None):
     (32, 4, 4, 128, torch.bfloat16),    # G 8 x 4: 32 columns (four tiles)
     (8, 8, 5, 128, torch.float16),      # G 1 x 5: one tile
     (16, 8, 5, 128, torch.bfloat16),    # G 2 x 5: 10 columns (the 16-column tensor-core kernel)
+    (32, 8, 2, 128, torch.bfloat16),    # G 4 x 2: 8 columns, the narrowest softmax
+    (32, 8, 8, 128, torch.float16),     # G 4 x 8: 32 columns
     (16, 8, 5, 64, torch.bfloat16),     # G 2 x 5: two tiles, D 64
     (12, 4, 8, 64, torch.float16),      # G 3 x 8: 24 columns, D 64
     (32, 8, 1, 128, torch.bfloat16),    # q_len 1 is decode
