@@ -23,6 +23,7 @@ from .kv_int8 import (  # noqa: F401,E402
     dequantize_rows_int8,
     gather_dequantized,
     quantize_rows_int8,
+    verify_int8_ref,
 )
 from .rope import append_rope_ref, rope_cache_ref, rope_inv_freq, rope_rotate_ref  # noqa: F401,E402
 from .block_manager import BlockManagerRef, NoBlocks, block_key, fnv1a64  # noqa: F401,E402

@@ -18,6 +18,11 @@ x_q = round(x / s), x_hat = s * x_q):
   with each new (token, head) row quantised on the way into the pool.
 * ``decode_int8_ref`` -- decode attention over the dequantised cache: the
   float oracle's softmax(scale * q K_hat^T) V_hat, in float64.
+* ``verify_int8_ref`` -- the verification pass of speculative decoding over
+  the same cache ("LLM Inference Server", *Batched Scheduling & Speculative
+  Decoding*: the target model checks the K drafted tokens in one pass, q_len =
+  K + 1 query tokens per sequence): query i of a sequence with context c sits
+  at position c - q_len + i and attends the dequantised keys 0..that position.
 
 Layout: codes ``int8 [num_blocks][H_kv][16][D]`` (the float pool's layout),
 scales ``float32 [num_blocks][H_kv][16]`` (one per token slot and head).
@@ -104,4 +109,25 @@ def decode_int8_ref(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray, k_s
         k = gather_dequantized(k_codes, k_scales, block_tables[s], c)
         v = gather_dequantized(v_codes, v_scales, block_tables[s], c)
         out[s] = attend(q64[s], k, v, scale, c)
+    return out
+
+
+def verify_int8_ref(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray, k_scales: np.ndarray,
+                    v_scales: np.ndarray, block_tables: np.ndarray, context_lens: np.ndarray,
+                    scale: float, seqs=None) -> np.ndarray:
+    """q: [S][q_len][H_q][D] (bf16 bits, fp16 or fp32), the last accepted token
+    and the drafted ones of each sequence, all already in the cache.  Returns
+    float64 [S][q_len][H_q][D]; a query whose position is negative (context
+    shorter than q_len) sees no key and gives a zero row.  Rows of sequences
+    not in ``seqs`` stay zero when a subset is asked for."""
+    q64 = as_f64(q)
+    S, q_len, h_q, d = q64.shape
+    out = np.zeros((S, q_len, h_q, d), dtype=np.float64)
+    for s in (range(S) if seqs is None else seqs):
+        c = int(context_lens[s])
+        k = gather_dequantized(k_codes, k_scales, block_tables[s], c)
+        v = gather_dequantized(v_codes, v_scales, block_tables[s], c)
+        for i in range(q_len):
+            pos = c - q_len + i
+            out[s, i] = attend(q64[s, i], k, v, scale, max(pos + 1, 0))
     return out

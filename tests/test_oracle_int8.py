@@ -9,8 +9,11 @@ reconstruction error is at most s / 2, power-of-two scaling commutes).  The
 INT8 decode is checked against the pinned float oracle on pools whose values
 are exactly representable as code x scale, against a pure-Python walk of the
 code and scale pools, and against the error bound that V quantisation
-implies.  The last group plants plausible mistakes and checks that the pins
-catch them.
+implies.  The INT8 verification pass is checked against the decode oracle at
+q_len = 1, the pinned float prompt pass on exactly representable pools, a
+torch float64 masked softmax over rows walked out of the pools, and the one-key
+case of a fresh context.  The last group plants plausible mistakes and checks
+that the pins catch them.
 """
 from __future__ import annotations
 
@@ -264,6 +267,85 @@ def test_v_quantisation_error_is_bounded():
 
 
 # ---------------------------------------------------------------------------
+# verification pass (q_len query tokens per sequence, causal)
+# ---------------------------------------------------------------------------
+
+def test_verify_int8_with_one_query_is_decode():
+    """q_len = 1: the only query sits at position c - 1 and sees the whole
+    context, which is the decode oracle's computation."""
+    nb, h, hq, d = 16, 2, 8, 16
+    kc, vc, ks, vs = _int8_pools(40, nb, h, d)
+    ctx = [1, 30, 64, 0]
+    bt = _tables(41, nb, ctx)
+    q = torch.randn((4, hq, d), generator=torch.Generator().manual_seed(42)).numpy()
+    want = oracle.decode_int8_ref(q, kc, vc, ks, vs, bt, np.array(ctx), 0.3)
+    got = oracle.verify_int8_ref(q[:, None], kc, vc, ks, vs, bt, np.array(ctx), 0.3)
+    assert np.array_equal(got[:, 0], want)
+
+
+def test_verify_int8_equals_float_prefill_on_exact_pools():
+    """On pools that hold x_hat = s * x_q exactly, the verification pass is the
+    pinned float prompt pass over a cached prefix with q_len new rows per
+    sequence (bit for bit in float64), including a context shorter than q_len."""
+    nb, h, hq, d, ql = 24, 2, 8, 16, 5
+    kc, vc, ks, vs = _int8_pools(43, nb, h, d, pow2_scales=True)
+    ctx = [5, 17, 3, 90]
+    bt = _tables(44, nb, ctx)
+    q = torch.randn((len(ctx), ql, hq, d), generator=torch.Generator().manual_seed(45)).numpy()
+    kf = ks[..., None].astype(np.float64) * kc.astype(np.float64)
+    vf = vs[..., None].astype(np.float64) * vc.astype(np.float64)
+    cu = np.arange(len(ctx) + 1, dtype=np.int64) * ql
+    want = oracle.prefill_ref(q.reshape(-1, hq, d), kf, vf, bt, cu, np.array(ctx), 0.25)
+    got = oracle.verify_int8_ref(q, kc, vc, ks, vs, bt, np.array(ctx), 0.25)
+    assert np.array_equal(got.reshape(-1, hq, d), want)
+
+
+def test_verify_int8_against_masked_softmax_from_pools():
+    """Each sequence's K_hat and V_hat built by walking the block table and the
+    code and scale pools in plain Python; all q_len x H_q scores at once in
+    torch float64 with a causal mask (query i may see key j iff
+    j <= c - q_len + i); fully masked rows are zero."""
+    nb, h, hq, d, ql = 12, 2, 4, 8, 4
+    kc, vc, ks, vs = _int8_pools(46, nb, h, d)
+    ctx = [4, 2, 37, 16]
+    bt = _tables(47, nb, ctx)
+    q = torch.randn((len(ctx), ql, hq, d), generator=torch.Generator().manual_seed(48), dtype=torch.float64)
+    got = oracle.verify_int8_ref(q.numpy(), kc, vc, ks, vs, bt, np.array(ctx), 0.35)
+    G = hq // h
+    for s, c in enumerate(ctx):
+        kh = torch.zeros((c, h, d), dtype=torch.float64)
+        vh = torch.zeros((c, h, d), dtype=torch.float64)
+        for p in range(c):
+            b, o = int(bt[s][p // BS]), p % BS
+            for g in range(h):
+                for e in range(d):
+                    kh[p, g, e] = float(ks[b, g, o]) * int(kc[b, g, o, e])
+                    vh[p, g, e] = float(vs[b, g, o]) * int(vc[b, g, o, e])
+        allowed = torch.tensor([[j <= c - ql + i for j in range(c)] for i in range(ql)], dtype=torch.bool)
+        for hh in range(hq):
+            x = 0.35 * q[s, :, hh, :] @ kh[:, hh // G, :].T                 # [q_len][c]
+            x = x.masked_fill(~allowed, float("-inf"))
+            w = torch.softmax(x, dim=-1).nan_to_num(0.0)                      # all-masked rows -> 0
+            want = (w @ vh[:, hh // G, :]).numpy()
+            assert np.max(np.abs(got[s, :, hh, :] - want)) < 1e-12
+
+
+def test_verify_int8_first_query_of_a_fresh_context_sees_one_key():
+    """c = q_len: query 0 sits at position 0, so its output is V_hat of slot 0
+    of the first block, whatever q holds."""
+    nb, h, hq, d, ql = 6, 2, 4, 8, 5
+    kc, vc, ks, vs = _int8_pools(49, nb, h, d)
+    bt = _tables(50, nb, [ql])
+    q = torch.randn((1, ql, hq, d), generator=torch.Generator().manual_seed(51)).numpy() * 7.0
+    got = oracle.verify_int8_ref(q, kc, vc, ks, vs, bt, np.array([ql]), 1.0)
+    b = int(bt[0, 0])
+    for hh in range(hq):
+        g = hh // (hq // h)
+        v0 = float(vs[b, g, 0]) * vc[b, g, 0].astype(np.float64)
+        assert np.allclose(got[0, 0, hh], v0, rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes
 # ---------------------------------------------------------------------------
 
@@ -313,3 +395,16 @@ def test_planted_scale_transpose_is_caught(monkeypatch):
     monkeypatch.setattr(q8, "gather_dequantized", gather)
     with pytest.raises(AssertionError):
         test_decode_int8_equals_float_oracle_on_exact_pools()
+
+
+@pytest.mark.parametrize("shift", [-1, 1])
+def test_planted_causal_offset_is_caught(shift, monkeypatch):
+    """A query that sees one key too few or one too many."""
+    real = q8.attend
+
+    def attend(q_row, k, v, scale, n_keys, return_lse=False):
+        n = min(max(n_keys + shift, 0), k.shape[0])
+        return real(q_row, k, v, scale, n, return_lse)
+    monkeypatch.setattr(q8, "attend", attend)
+    with pytest.raises(AssertionError):
+        test_verify_int8_against_masked_softmax_from_pools()
