@@ -51,7 +51,8 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD,
                    help="llama3_8b_decode (the headline line) or one of tiny_fp32, llama32_1b_decode, "
                         "prefix_shared_8k, mixed_mistral7b, llama32_1b_decode_int8, llama3_8b_decode_int8, "
-                        "llama3_8b_verify, llama3_8b_decode_rope (per-call figures for that workload), or "
+                        "llama3_8b_verify, llama3_8b_verify_int8, llama3_8b_decode_rope (per-call figures for that "
+                        "workload), or "
                         "llama3_8b_prefix_serving (decode steps driven by the block manager)")
     p.add_argument("--quick", action="store_true",
                    help="no CPU baseline, no 1 s pre-warm, no end-to-end pass (for profiler runs)")
@@ -593,7 +594,11 @@ def run_other(args):
                                     max_q_len=max(wl.prompt_lens), max_context_len=max(wl.prompt_lens),
                                     stream=stream)
         evs[2].record(stream)
-        if vq:
+        if vq and wl.kv_int8:
+            pa.pa_verify_attention_int8(out, d["vq"], kp, vp, ks, vs, bt, d["ctx"], wl.scale,
+                                        max_context_len=max_ctx, partition_size=args.partition, workspace=ws,
+                                        stream=stream)
+        elif vq:
             pa.pa_verify_attention(out, d["vq"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
                                    partition_size=args.partition, workspace=ws, stream=stream)
         elif wl.kv_int8:

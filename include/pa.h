@@ -313,6 +313,32 @@ PA_API int pa_decode_attention_int8(void* out, const void* q, const void* k_code
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_verify_attention_int8 -- pa_verify_attention over an INT8 cache: q_len
+ * query tokens per sequence (the last accepted token and the drafted ones of
+ * "LLM Inference Server", Batched Scheduling & Speculative Decoding), query i
+ * at position context_lens[s] - q_len + i attending the dequantised keys
+ * 0..that position, as pa_decode_attention_int8 does for one query.  The code
+ * and scale blocks of a KV head are read once for all q_len x G query rows;
+ * long contexts split into partitions of partition_size tokens merged by
+ * log-sum-exp.  q_len = 1 is pa_decode_attention_int8.
+ *
+ *   out, q        : [num_seqs][q_len][num_q_heads][D], act_dtype
+ *   context_lens  : rows whose position is negative see no key and are zero
+ *   workspace     : >= pa_verify_workspace_size(..., pool) bytes with
+ *                   pool->dtype = PA_I8, zero-filled before its first use
+ * Errors as pa_decode_attention_int8, plus PA_ERR_INVALID for q_len < 1 and
+ * PA_ERR_UNSUPPORTED for (num_q_heads/num_kv_heads) * q_len > 32.
+ */
+PA_API int pa_verify_attention_int8(void* out, const void* q, const void* k_codes,
+                                    const void* v_codes, const float* k_scales,
+                                    const float* v_scales, const int32_t* block_tables,
+                                    const int32_t* context_lens, float scale, int num_seqs,
+                                    int q_len, int num_q_heads, int max_blocks_per_seq,
+                                    int max_context_len, int partition_size, int act_dtype,
+                                    const pa_pool_desc* pool, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
  * Rotary position embedding fused into the append.  The pages name RoPE as a
  * step to fuse with attention ("Mini inference engine", Story / portfolio:
  * fuse qkv_proj + RoPE + attention) without defining it; this is the

@@ -113,6 +113,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_attention_int8.restype = i32
     L.pa_decode_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
                                            pdesc, vp, sz, vp]
+    L.pa_verify_attention_int8.restype = i32
+    L.pa_verify_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
+                                           i32, pdesc, vp, sz, vp]
     _lib = L
     return L
 
@@ -430,6 +433,37 @@ def pa_decode_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.
                                       _act(q), ctypes.byref(desc), _ptr(workspace), int(ws_bytes),
                                       _stream(stream)))
 
+
+
+def pa_verify_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                             k_scales: torch.Tensor, v_scales: torch.Tensor, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, scale: float, max_context_len: int,
+                             partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                             stream=None) -> None:
+    """pa_verify_attention over an INT8 cache; out, q: [S][q_len][H_q][D]
+    bf16/fp16, the last q_len positions of each sequence (already appended),
+    each attending causally to the cache.  ``workspace`` as in
+    pa_verify_attention (sized with the int8 code pool)."""
+    desc = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 4 and q.shape[3] == k_codes.shape[3], "q must be [S][q_len][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out/q shape or dtype mismatch")
+    S, ql, hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    _need(context_lens.dtype == torch.int32 and tuple(context_lens.shape) == (S,), "context_lens must be int32 [S]")
+    L = load_library()
+    if workspace is None:
+        need = pa_verify_workspace_size(S, ql, hq, max_context_len, k_codes, partition_size)
+        if need > 0:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.pa_verify_attention_int8(_ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+                                      _ptr(v_scales), _ptr(block_tables), _ptr(context_lens), float(scale), S, ql,
+                                      hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+                                      _act(q), ctypes.byref(desc), _ptr(workspace), int(ws_bytes),
+                                      _stream(stream)))
 
 # ---------------------------------------------------------------------------
 # rotary position embedding (half-split, Llama form)

@@ -110,8 +110,11 @@ template <> struct VRun<64> {
 
 }  // namespace
 
-template <typename T, int D, int W, int NS>
-__global__ void __launch_bounds__(W * 32, 4)
+// NT 8-column tiles of query columns (column c = i * G + h for query position
+// i and head h, as in decode_merge.cuh); CAUSAL masks key j from query i
+// unless j <= ctx - q_len + i.  Decode is NT = 1 without the mask.
+template <typename T, int D, int W, int NS, int NT, bool CAUSAL>
+__global__ void __launch_bounds__(W * 32, NT == 1 ? 4 : 2)
 decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                  const DecodeArgs a) {
   constexpr int TILE = 16 * D;         // one (block, head) tile of codes
@@ -119,6 +122,7 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   constexpr int KS = D / 16;           // k-steps of the score MMA = m-tiles of the PV MMA
   constexpr int HALVES = D / 64;       // 64-entry halves of the head dim
   constexpr int RUNW = VRun<D>::WORDS; // words of a lane's V run
+  constexpr int NC = 8 * NT;           // query columns per warp state
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[W * NS];
@@ -132,6 +136,7 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = a.num_q_heads / a.num_kv_heads;
+  const int ncols = CAUSAL ? G * a.q_len : G;
 
   grid_dependency_wait();   // the codes may come from the append just before us
   const int ctx = checked_context(a, s, threadIdx.x == 0 && split == 0 && kvh == 0);
@@ -194,14 +199,19 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const int c = lane & 3;    // thread in group
 
   // ---- q in fp16, exactly, with a power-of-two row scale ---------------------
-  // B operand of the score MMA: k-step ks = 4 h + j holds, for this lane,
-  // q[g][64 h + 16 c + 4 j + (0, 1)] and (+2, +3).
-  uint32_t qf[KS][2];
-  float f_head;   // scale * log2(e) * 2^-e of query head g
-  {
+  // B operand of the score MMA: k-step ks = 4 h + j of tile nt holds, for this
+  // lane, q[column 8 nt + g][64 h + 16 c + 4 j + (0, 1)] and (+2, +3).
+  uint32_t qf[NT][KS][2];
+  float f0[NT], f1[NT];   // scale * log2(e) * 2^-e of this lane's score columns 2c, 2c+1
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = 8 * nt + g;
     float qv[HALVES * 16];
-    if (g < G) {
-      const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(s) * a.num_q_heads + kvh * G + g) * D;
+    if (col < ncols) {
+      const int qi = col / G;
+      const int h = col - qi * G;
+      const T* qrow = static_cast<const T*>(a.q) +
+                      ((static_cast<size_t>(s) * a.q_len + qi) * a.num_q_heads + kvh * G + h) * D;
 #pragma unroll
       for (int hf = 0; hf < HALVES; ++hf) {
         const uint4* p = reinterpret_cast<const uint4*>(qrow + 64 * hf + 16 * c);
@@ -228,37 +238,57 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       e = e > 126 ? 126 : (e < -126 ? -126 : e);
     }
     const float up = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-    f_head = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    const float f_head = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 #pragma unroll
     for (int hf = 0; hf < HALVES; ++hf) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float* v = qv + hf * 16 + 4 * j;
-        qf[hf * 4 + j][0] = pack_half2(v[0] * up, v[1] * up);
-        qf[hf * 4 + j][1] = pack_half2(v[2] * up, v[3] * up);
+        qf[nt][hf * 4 + j][0] = pack_half2(v[0] * up, v[1] * up);
+        qf[nt][hf * 4 + j][1] = pack_half2(v[2] * up, v[3] * up);
       }
     }
+    f0[nt] = __shfl_sync(0xffffffffu, f_head, 8 * c);
+    f1[nt] = __shfl_sync(0xffffffffu, f_head, 8 * c + 4);
   }
-  // this lane's score columns are query heads 2c and 2c+1
-  const float f0 = __shfl_sync(0xffffffffu, f_head, 8 * c);
-  const float f1 = __shfl_sync(0xffffffffu, f_head, 8 * c + 4);
   const uint32_t cbias[4] = {kBiasPair, kBiasPair, kBiasPair, kBiasPair};
-  float bq[4] = {0.f, 0.f, 0.f, 0.f};   // 1152 * sum_d q16[head][d]: [0],[2] head 2c; [1],[3] head 2c+1
+  // 1152 * sum_d q16[column][d]: [0],[2] column 2c; [1],[3] column 2c+1 of each tile
+  float bq[NT][4];
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) Mma<__half>::run(bq, cbias, qf[ks][0], qf[ks][1]);
+  for (int nt = 0; nt < NT; ++nt) {
+    bq[nt][0] = bq[nt][1] = bq[nt][2] = bq[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) Mma<__half>::run(bq[nt], cbias, qf[nt][ks][0], qf[nt][ks][1]);
+  }
+  // keys visible to this lane's score columns: ctx - q_len + 1 + i for query
+  // position i, none for padding columns
+  int lim[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int col = 8 * nt + 2 * c + u;
+      lim[nt][u] = CAUSAL ? (col < ncols ? ctx - a.q_len + 1 + col / G : 0) : ctx;
+    }
+  }
 
-  // Softmax state of query heads 2c, 2c+1 in the log2 domain.  m_ref is a
+  // Softmax state of this lane's columns in the log2 domain.  m_ref is a
   // lazily raised reference: it moves only when a score exceeds it by more
   // than kLazy, so unnormalised weights stay <= 2^kLazy and most blocks need
   // no reduction and no rescale.  sv_ref plays the same role for the V scales.
-  float m_ref[2] = {-INFINITY, -INFINITY};
-  float mu[2] = {0.f, 0.f};             // m_ref, or 0 while it is -inf
-  float l_run[2] = {0.f, 0.f};          // this lane's share of sum 2^(x - m_ref)
+  float m_ref[NT][2], mu[NT][2], l_run[NT][2];   // mu: m_ref, or 0 while it is -inf
   float sv_ref = 0.f, sv_inv = 0.f;
-  float acc[KS][4];
-  float bo[4] = {0.f, 0.f, 0.f, 0.f};   // 1152 * sum_i p''_i, accumulated like O
+  float acc[NT][KS][4];
+  float bo[NT][4];   // 1152 * sum_i p''_i, accumulated like O
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt) {
+    m_ref[nt][0] = m_ref[nt][1] = -INFINITY;
+    mu[nt][0] = mu[nt][1] = 0.f;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+    bo[nt][0] = bo[nt][1] = bo[nt][2] = bo[nt][3] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
+  }
 
   const int r0 = tau(g), r1 = tau(g + 8);                    // token rows of the score accumulators
   const int tx = tau(2 * c), ty = tau(2 * c + 1);            // tokens of PV k-slots 2c, 2c+1
@@ -283,8 +313,12 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     if (bad_mask & (1u << i)) nvalid = 0;
 
     // ---- scores -----------------------------------------------------------
-    float sa[4] = {0.f, 0.f, 0.f, 0.f};
-    float sb[4] = {0.f, 0.f, 0.f, 0.f};
+    float sa[NT][4], sb[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      sa[nt][0] = sa[nt][1] = sa[nt][2] = sa[nt][3] = 0.f;
+      sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
+    }
 #pragma unroll
     for (int hf = 0; hf < HALVES; ++hf) {
       uint4 A = lds128(kt + tile_chunk<D>(r0, 4 * hf + c));
@@ -295,10 +329,13 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       for (int j = 0; j < 4; ++j) {
         const uint32_t af[4] = {widen(wa[j], 0x4140), widen(wb[j], 0x4140), widen(wa[j], 0x4342),
                                 widen(wb[j], 0x4342)};
-        if (j & 1)
-          Mma<__half>::run(sb, af, qf[hf * 4 + j][0], qf[hf * 4 + j][1]);
-        else
-          Mma<__half>::run(sa, af, qf[hf * 4 + j][0], qf[hf * 4 + j][1]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (j & 1)
+            Mma<__half>::run(sb[nt], af, qf[nt][hf * 4 + j][0], qf[nt][hf * 4 + j][1]);
+          else
+            Mma<__half>::run(sa[nt], af, qf[nt][hf * 4 + j][0], qf[nt][hf * 4 + j][1]);
+        }
       }
     }
     const bool v0 = r0 < nvalid, v1 = r1 < nvalid;
@@ -306,57 +343,78 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const float sk1 = v1 ? sk[r1] : 0.f;
     const float sv0 = v0 ? sv[r0] : 0.f;
     const float sv1 = v1 ? sv[r1] : 0.f;
-    const float x0 = v0 ? (sa[0] + sb[0] - bq[0]) * (f0 * sk0) : -INFINITY;
-    const float x1 = v0 ? (sa[1] + sb[1] - bq[1]) * (f1 * sk0) : -INFINITY;
-    const float x2 = v1 ? (sa[2] + sb[2] - bq[2]) * (f0 * sk1) : -INFINITY;
-    const float x3 = v1 ? (sa[3] + sb[3] - bq[3]) * (f1 * sk1) : -INFINITY;
+    float x[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      bool m0 = v0, m1 = v0, m2 = v1, m3 = v1;   // (token r0 | r1) x (column 2c | 2c+1)
+      if (CAUSAL) {
+        const int base = lb * kBlock;
+        m0 = v0 && r0 < lim[nt][0] - base;
+        m1 = v0 && r0 < lim[nt][1] - base;
+        m2 = v1 && r1 < lim[nt][0] - base;
+        m3 = v1 && r1 < lim[nt][1] - base;
+      }
+      x[nt][0] = m0 ? (sa[nt][0] + sb[nt][0] - bq[nt][0]) * (f0[nt] * sk0) : -INFINITY;
+      x[nt][1] = m1 ? (sa[nt][1] + sb[nt][1] - bq[nt][1]) * (f1[nt] * sk0) : -INFINITY;
+      x[nt][2] = m2 ? (sa[nt][2] + sb[nt][2] - bq[nt][2]) * (f0[nt] * sk1) : -INFINITY;
+      x[nt][3] = m3 ? (sa[nt][3] + sb[nt][3] - bq[nt][3]) * (f1[nt] * sk1) : -INFINITY;
+    }
 
     // ---- raise the references (rare) -----------------------------------------
-    const bool grow = fmaxf(x0, x2) > m_ref[0] + kLazy || fmaxf(x1, x3) > m_ref[1] + kLazy ||
-                      fmaxf(sv0, sv1) > sv_ref;
+    bool grow = fmaxf(sv0, sv1) > sv_ref;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      grow = grow || fmaxf(x[nt][0], x[nt][2]) > m_ref[nt][0] + kLazy ||
+             fmaxf(x[nt][1], x[nt][3]) > m_ref[nt][1] + kLazy;
     if (__any_sync(0xffffffffu, grow)) {
-      const float mb0 = warp_max_xor(fmaxf(x0, x2), 4, 16);
-      const float mb1 = warp_max_xor(fmaxf(x1, x3), 4, 16);
       const float svb = warp_max_xor(fmaxf(sv0, sv1), 4, 16);
-      const float mn0 = fmaxf(m_ref[0], mb0);
-      const float mn1 = fmaxf(m_ref[1], mb1);
       const float svn = svb > sv_ref ? 2.f * svb : sv_ref;   // headroom: fewer raises
       const float rs = svn > 0.f ? sv_ref / svn : 1.f;
-      const float al0 = fast_exp2(m_ref[0] - (mn0 == -INFINITY ? 0.f : mn0));
-      const float al1 = fast_exp2(m_ref[1] - (mn1 == -INFINITY ? 0.f : mn1));
-      l_run[0] *= al0;
-      l_run[1] *= al1;
-      const float be0 = al0 * rs, be1 = al1 * rs;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        acc[mt][0] *= be0;
-        acc[mt][1] *= be1;
-        acc[mt][2] *= be0;
-        acc[mt][3] *= be1;
+      for (int nt = 0; nt < NT; ++nt) {
+        const float mb0 = warp_max_xor(fmaxf(x[nt][0], x[nt][2]), 4, 16);
+        const float mb1 = warp_max_xor(fmaxf(x[nt][1], x[nt][3]), 4, 16);
+        const float mn0 = fmaxf(m_ref[nt][0], mb0);
+        const float mn1 = fmaxf(m_ref[nt][1], mb1);
+        const float al0 = fast_exp2(m_ref[nt][0] - (mn0 == -INFINITY ? 0.f : mn0));
+        const float al1 = fast_exp2(m_ref[nt][1] - (mn1 == -INFINITY ? 0.f : mn1));
+        l_run[nt][0] *= al0;
+        l_run[nt][1] *= al1;
+        const float be0 = al0 * rs, be1 = al1 * rs;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          acc[nt][mt][0] *= be0;
+          acc[nt][mt][1] *= be1;
+          acc[nt][mt][2] *= be0;
+          acc[nt][mt][3] *= be1;
+        }
+        bo[nt][0] *= be0;
+        bo[nt][1] *= be1;
+        bo[nt][2] *= be0;
+        bo[nt][3] *= be1;
+        m_ref[nt][0] = mn0;
+        m_ref[nt][1] = mn1;
+        mu[nt][0] = mn0 == -INFINITY ? 0.f : mn0;
+        mu[nt][1] = mn1 == -INFINITY ? 0.f : mn1;
       }
-      bo[0] *= be0;
-      bo[1] *= be1;
-      bo[2] *= be0;
-      bo[3] *= be1;
-      m_ref[0] = mn0;
-      m_ref[1] = mn1;
-      mu[0] = mn0 == -INFINITY ? 0.f : mn0;
-      mu[1] = mn1 == -INFINITY ? 0.f : mn1;
       sv_ref = svn;
       sv_inv = svn > 0.f ? __frcp_rn(svn) : 0.f;
     }
-    const float p0 = fast_exp2(x0 - mu[0]);
-    const float p1 = fast_exp2(x1 - mu[1]);
-    const float p2 = fast_exp2(x2 - mu[0]);
-    const float p3 = fast_exp2(x3 - mu[1]);
-    l_run[0] += p0 + p2;
-    l_run[1] += p1 + p3;
     const float w0 = sv0 * sv_inv, w1 = sv1 * sv_inv;   // s_v / sv_ref in [0, 1/2]
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float p0 = fast_exp2(x[nt][0] - mu[nt][0]);
+      const float p1 = fast_exp2(x[nt][1] - mu[nt][1]);
+      const float p2 = fast_exp2(x[nt][2] - mu[nt][0]);
+      const float p3 = fast_exp2(x[nt][3] - mu[nt][1]);
+      l_run[nt][0] += p0 + p2;
+      l_run[nt][1] += p1 + p3;
+      pb0[nt] = movmatrix_trans(pack_half2(p0 * w0, p1 * w0));
+      pb1[nt] = movmatrix_trans(pack_half2(p2 * w1, p3 * w1));
+    }
 
-    const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * w0, p1 * w0));
-    const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * w1, p3 * w1));
-
-    // ---- O^T[d][head] += V^T[d][token] P^T[token][head] ----------------------
+    // ---- O^T[d][column] += V^T[d][token] P^T[token][column] ------------------
     uint32_t X[RUNW], Y[RUNW], Z[RUNW], Wr[RUNW];
     VRun<D>::load(vt, tx, g, X);
     VRun<D>::load(vt, ty, g, Y);
@@ -368,9 +426,11 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       const uint32_t t0 = __byte_perm(X[mt >> 1], Y[mt >> 1], sel);
       const uint32_t t1 = __byte_perm(Z[mt >> 1], Wr[mt >> 1], sel);
       const uint32_t vf[4] = {widen(t0, 0x4140), widen(t0, 0x4342), widen(t1, 0x4140), widen(t1, 0x4342)};
-      Mma<__half>::run(acc[mt], vf, pb0, pb1);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(acc[nt][mt], vf, pb0[nt], pb1[nt]);
     }
-    Mma<__half>::run(bo, cbias, pb0, pb1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(bo[nt], cbias, pb0[nt], pb1[nt]);
 
     __syncwarp();
     if (i + NS < nb_w) {
@@ -385,61 +445,80 @@ decode_q8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     for (int j = i; j < last; ++j) mbar_wait_bounded(bar0 + 8 * (j % NS), (j / NS) & 1, 100000000ull);
   }
 
-  l_run[0] = warp_sum_xor(l_run[0], 4, 16);
-  l_run[1] = warp_sum_xor(l_run[1], 4, 16);
-
   // ---- merge the W warp states through shared memory -------------------------
   __syncthreads();
   float* red_o = reinterpret_cast<float*>(smem);
-  float* red_m = red_o + W * 8 * D;
-  float* red_l = red_m + W * 8;
-  const int h0 = 2 * c;
-  const int h1 = 2 * c + 1;
+  float* red_m = red_o + W * NC * D;
+  float* red_l = red_m + W * NC;
   constexpr int RUN = D / 8;
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
-    const int d0 = RUN * g + 2 * mt;
-    if (h0 < G) {
-      red_o[(warp * 8 + h0) * D + d0] = (acc[mt][0] - bo[0]) * sv_ref;
-      red_o[(warp * 8 + h0) * D + d0 + 1] = (acc[mt][2] - bo[2]) * sv_ref;
+  for (int nt = 0; nt < NT; ++nt) {
+    l_run[nt][0] = warp_sum_xor(l_run[nt][0], 4, 16);
+    l_run[nt][1] = warp_sum_xor(l_run[nt][1], 4, 16);
+    const int h0 = 8 * nt + 2 * c;
+    const int h1 = h0 + 1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      const int d0 = RUN * g + 2 * mt;
+      if (h0 < ncols) {
+        red_o[(warp * NC + h0) * D + d0] = (acc[nt][mt][0] - bo[nt][0]) * sv_ref;
+        red_o[(warp * NC + h0) * D + d0 + 1] = (acc[nt][mt][2] - bo[nt][2]) * sv_ref;
+      }
+      if (h1 < ncols) {
+        red_o[(warp * NC + h1) * D + d0] = (acc[nt][mt][1] - bo[nt][1]) * sv_ref;
+        red_o[(warp * NC + h1) * D + d0 + 1] = (acc[nt][mt][3] - bo[nt][3]) * sv_ref;
+      }
     }
-    if (h1 < G) {
-      red_o[(warp * 8 + h1) * D + d0] = (acc[mt][1] - bo[1]) * sv_ref;
-      red_o[(warp * 8 + h1) * D + d0 + 1] = (acc[mt][3] - bo[3]) * sv_ref;
-    }
-  }
-  if (g == 0) {
-    if (h0 < G) {
-      red_m[warp * 8 + h0] = m_ref[0];
-      red_l[warp * 8 + h0] = l_run[0];
-    }
-    if (h1 < G) {
-      red_m[warp * 8 + h1] = m_ref[1];
-      red_l[warp * 8 + h1] = l_run[1];
+    if (g == 0) {
+      if (h0 < ncols) {
+        red_m[warp * NC + h0] = m_ref[nt][0];
+        red_l[warp * NC + h0] = l_run[nt][0];
+      }
+      if (h1 < ncols) {
+        red_m[warp * NC + h1] = m_ref[nt][1];
+        red_l[warp * NC + h1] = l_run[nt][1];
+      }
     }
   }
   __syncthreads();
-  cta_merge_store<T, W, D>(a, red_o, red_m, red_l, G, s, kvh, split, n_splits);
+  cta_merge_store<T, W, D, NC>(a, red_o, red_m, red_l, G, s, kvh, split, n_splits);
 }
 
 namespace {
 
-template <typename T, int D>
+template <typename T, int D, int NT, bool CAUSAL>
 cudaError_t launch_q8_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         cudaStream_t stream) {
   constexpr int W = 4;
-  // 48 KB of stages per CTA: 4 CTAs (16 warps) per SM.  The loop is bound by
-  // instruction issue, so more warps per SM beat deeper per-warp pipelines
-  // (the same bytes in flight with 4 stages and 3 CTAs ran ~9% slower).
-  constexpr int NS = (D == 128) ? 3 : 6;
+  // Decode: 48 KB of stages per CTA, 4 CTAs (16 warps) per SM.  The loop is
+  // bound by instruction issue, so more warps per SM beat deeper per-warp
+  // pipelines (the same bytes in flight with 4 stages and 3 CTAs ran ~9%
+  // slower).  Wider query tiles hold more accumulators per thread and run 2
+  // CTAs per SM with one more stage each.
+  constexpr int NS = NT == 1 ? ((D == 128) ? 3 : 6) : ((D == 128) ? 4 : 8);
   constexpr int STAGE = 2 * 16 * D;
-  static_assert(W * 8 * D * 4 + W * 16 * 4 <= W * NS * STAGE, "merge buffer must fit");
-  const int smem = W * NS * STAGE + 1024;
-  auto kern = decode_q8_kernel<T, D, W, NS>;
+  constexpr int NC = 8 * NT;
+  constexpr int MERGE = W * NC * D * 4 + 2 * W * NC * 4;
+  constexpr int BODY = W * NS * STAGE > MERGE ? W * NS * STAGE : MERGE;
+  const int smem = BODY + 1024;
+  auto kern = decode_q8_kernel<T, D, W, NS, NT, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
   return launch_pdl(kern, grid, dim3(W * 32), smem, stream, kmap, vmap, a);
+}
+
+template <typename T, int D>
+cudaError_t launch_q8_d(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        cudaStream_t stream) {
+  if (a.q_len == 1) return launch_q8_t<T, D, 1, false>(a, kmap, vmap, stream);
+  const int tiles = ((a.num_q_heads / a.num_kv_heads) * a.q_len + 7) / 8;   // <= 4 (host limit)
+  switch (tiles) {
+    case 1: return launch_q8_t<T, D, 1, true>(a, kmap, vmap, stream);
+    case 2: return launch_q8_t<T, D, 2, true>(a, kmap, vmap, stream);
+    case 3: return launch_q8_t<T, D, 3, true>(a, kmap, vmap, stream);
+    default: return launch_q8_t<T, D, 4, true>(a, kmap, vmap, stream);
+  }
 }
 
 }  // namespace
@@ -447,11 +526,11 @@ cudaError_t launch_q8_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUte
 cudaError_t launch_decode_q8(const DecodeArgs& a, int act_dtype, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t stream) {
   if (act_dtype == PA_BF16) {
-    return a.head_dim == 128 ? launch_q8_t<__nv_bfloat16, 128>(a, kmap, vmap, stream)
-                             : launch_q8_t<__nv_bfloat16, 64>(a, kmap, vmap, stream);
+    return a.head_dim == 128 ? launch_q8_d<__nv_bfloat16, 128>(a, kmap, vmap, stream)
+                             : launch_q8_d<__nv_bfloat16, 64>(a, kmap, vmap, stream);
   }
-  return a.head_dim == 128 ? launch_q8_t<__half, 128>(a, kmap, vmap, stream)
-                           : launch_q8_t<__half, 64>(a, kmap, vmap, stream);
+  return a.head_dim == 128 ? launch_q8_d<__half, 128>(a, kmap, vmap, stream)
+                           : launch_q8_d<__half, 64>(a, kmap, vmap, stream);
 }
 
 }  // namespace pa

@@ -125,14 +125,17 @@ int max_splits_for(int max_context_len, int part_blocks) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Verification on the tensor-core kernel: head dim 128 and more than one query position.
-bool verify_on_umma(int q_len, int head_dim) { return q_len > 1 && head_dim == 128; }
+// Verification on the tensor-core kernel: a float pool, head dim 128 and more
+// than one query position.
+bool verify_on_umma(int q_len, const pa_pool_desc* pool) {
+  return q_len > 1 && pool->head_dim == 128 && pool->dtype != PA_I8;
+}
 
 // Partial-output slots per query row of a verify call: the split-K partitions of
 // the mma.sync kernels, or the stream-K segments of the tensor-core kernel.
-int verify_slots(int q_len, int head_dim, int max_context_len, int part_blocks) {
-  return verify_on_umma(q_len, head_dim) ? pa::verify_umma_slots(max_context_len, part_blocks)
-                                         : max_splits_for(max_context_len, part_blocks);
+int verify_slots(int q_len, const pa_pool_desc* pool, int max_context_len, int part_blocks) {
+  return verify_on_umma(q_len, pool) ? pa::verify_umma_slots(max_context_len, part_blocks)
+                                     : max_splits_for(max_context_len, part_blocks);
 }
 
 // [counters: kCounterBytes][partial outputs: rows x D fp32][partial lse: rows fp32]
@@ -416,7 +419,7 @@ size_t pa_verify_workspace_size(int num_seqs, int q_len, int num_q_heads, int ma
     return 0;
   }
   const int p = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
-  const int ms = verify_slots(q_len, pool->head_dim, max_context_len, p / PA_BLOCK_SIZE);
+  const int ms = verify_slots(q_len, pool, max_context_len, p / PA_BLOCK_SIZE);
   return ws_layout(num_seqs * q_len, num_q_heads, ms, pool->head_dim).total;
 }
 
@@ -445,7 +448,7 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
 
   const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
   const int part_blocks = part / PA_BLOCK_SIZE;
-  const int max_splits = verify_slots(q_len, pool->head_dim, max_context_len, part_blocks);
+  const int max_splits = verify_slots(q_len, pool, max_context_len, part_blocks);
   const WsLayout ws = ws_layout(num_seqs * q_len, num_q_heads, max_splits, pool->head_dim);
   if (ws.total > 0 && static_cast<long long>(num_seqs) * pool->num_kv_heads > kMaxCounters)
     return fail(PA_ERR_UNSUPPORTED, "split-K over more than %d (sequence, KV head) pairs in one call",
@@ -486,7 +489,7 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = q_len == 1                                 ? pa::launch_decode_tc(a, pool->dtype, kmap, vmap, st)
-                  : verify_on_umma(q_len, pool->head_dim) ? pa::launch_verify_umma(a, pool->dtype, kmap, vmap, st)
+                  : verify_on_umma(q_len, pool) ? pa::launch_verify_umma(a, pool->dtype, kmap, vmap, st)
                                                             : pa::launch_verify_tc(a, pool->dtype, kmap, vmap, st);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return PA_OK;
@@ -564,15 +567,21 @@ int pa_append_kv_int8(void* k_codes, void* v_codes, float* k_scales, float* v_sc
   return PA_OK;
 }
 
-int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, const void* v_codes,
-                             const float* k_scales, const float* v_scales, const int32_t* block_tables,
-                             const int32_t* context_lens, float scale, int num_seqs, int num_q_heads,
-                             int max_blocks_per_seq, int max_context_len, int partition_size, int act_dtype,
-                             const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream) {
-  t_err.clear();
+namespace {
+// Decode (q_len = 1) and verification (q_len > 1) over an INT8 cache: one kernel
+// family, split-K partitions of partition_size tokens.
+int int8_attention(void* out, const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                   const float* v_scales, const int32_t* block_tables, const int32_t* context_lens, float scale,
+                   int num_seqs, int q_len, int num_q_heads, int max_blocks_per_seq, int max_context_len,
+                   int partition_size, int act_dtype, const pa_pool_desc* pool, void* workspace,
+                   size_t workspace_bytes, void* stream) {
   int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, pool);
   if (rc != PA_OK) return rc;
   if ((rc = check_int8(pool, act_dtype)) != PA_OK) return rc;
+  if (q_len < 1) return fail(PA_ERR_INVALID, "q_len must be >= 1");
+  if ((num_q_heads / pool->num_kv_heads) * q_len > 32)
+    return fail(PA_ERR_UNSUPPORTED, "query group x q_len = %d > 32", (num_q_heads / pool->num_kv_heads) * q_len);
+  if (static_cast<long long>(num_seqs) * q_len > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many rows");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_codes || !v_codes || !k_scales || !v_scales || !context_lens ||
@@ -587,7 +596,7 @@ int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, cons
   const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
   const int part_blocks = part / PA_BLOCK_SIZE;
   const int max_splits = max_splits_for(max_context_len, part_blocks);
-  const WsLayout ws = ws_layout(num_seqs, num_q_heads, max_splits, pool->head_dim);
+  const WsLayout ws = ws_layout(num_seqs * q_len, num_q_heads, max_splits, pool->head_dim);
   if (ws.total > 0 && static_cast<long long>(num_seqs) * pool->num_kv_heads > kMaxCounters)
     return fail(PA_ERR_UNSUPPORTED, "split-K over more than %d (sequence, KV head) pairs in one call",
                 kMaxCounters);
@@ -623,13 +632,36 @@ int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, cons
   a.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_off) : nullptr;
   a.ws_lse = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse_off) : nullptr;
   a.status = status;
-  a.q_len = 1;
+  a.q_len = q_len;
   CUtensorMap kmap, vmap;
   if ((rc = pool_map(&kmap, k_codes, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_codes, pool)) != PA_OK) return rc;
   cudaError_t e = pa::launch_decode_q8(a, act_dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "decode_int8 launch");
+  if (e != cudaSuccess) return cuda_fail(e, q_len == 1 ? "decode_int8 launch" : "verify_int8 launch");
   return PA_OK;
+}
+}  // namespace
+
+int pa_decode_attention_int8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                             const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, int num_seqs, int num_q_heads,
+                             int max_blocks_per_seq, int max_context_len, int partition_size, int act_dtype,
+                             const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  return int8_attention(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale, num_seqs,
+                        1, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, act_dtype, pool,
+                        workspace, workspace_bytes, stream);
+}
+
+int pa_verify_attention_int8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                             const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, int num_seqs, int q_len, int num_q_heads,
+                             int max_blocks_per_seq, int max_context_len, int partition_size, int act_dtype,
+                             const pa_pool_desc* pool, void* workspace, size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  return int8_attention(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale, num_seqs,
+                        q_len, num_q_heads, max_blocks_per_seq, max_context_len, partition_size, act_dtype, pool,
+                        workspace, workspace_bytes, stream);
 }
 
 int pa_rope_cache(float* cos_sin, int max_positions, int head_dim, double theta, void* stream) {

@@ -384,6 +384,7 @@ WORKLOADS = {
     "llama32_1b_decode_int8": lambda: llama32_1b_decode(kv="int8"),
     "llama3_8b_decode_int8": lambda: llama3_8b_decode(kv="int8"),
     "llama3_8b_verify": lambda: llama3_8b_verify(),
+    "llama3_8b_verify_int8": lambda: llama3_8b_verify(kv="int8"),
     "llama3_8b_decode_rope": lambda: llama3_8b_decode_rope(),
 }
 
@@ -399,13 +400,15 @@ def llama3_8b_decode_rope(steps: int = 32) -> Workload:
     return wl
 
 
-def llama3_8b_verify(steps: int = 32, q_len: int = 5) -> Workload:
+def llama3_8b_verify(steps: int = 32, q_len: int = 5, kv: str = "float") -> Workload:
     """The batch-64 Llama-3-8B-shaped decode batch in a speculative-decoding
     verification pass: each sequence's last q_len = K + 1 = 5 positions (K = 4
-    drafted tokens) are queries, causal over the cache."""
-    wl = llama3_8b_decode(steps=steps)
-    wl.name = "llama3_8b_verify"
-    wl.description = "Llama-3-8B-shaped verification of K=4 drafts (q_len 5), bf16, batch 64"
+    drafted tokens) are queries, causal over the cache.  ``kv="int8"``: the
+    same batch over an INT8 cache."""
+    wl = llama3_8b_decode(steps=steps, kv=kv)
+    wl.name = "llama3_8b_verify" + ("_int8" if kv == "int8" else "")
+    wl.description = ("Llama-3-8B-shaped verification of K=4 drafts (q_len 5), bf16, batch 64" +
+                      (", INT8 KV cache" if kv == "int8" else ""))
     wl.extra["verify_q_len"] = q_len
     return wl
 

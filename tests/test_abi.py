@@ -170,6 +170,31 @@ def test_int8_cache_entry_points_validate_on_the_host(lib):
         lib.pa_decode_workspace_size(64, 32, 8224, 0, ctypes.byref(_desc(d=128)))
 
 
+def _verify8(lib, desc, act=B.PA_BF16, ql=5, hq=32, maxc=100, part=512, S=4):
+    f = ctypes.c_void_p(FAKE)
+    return lib.pa_verify_attention_int8(f, f, f, f, f, f, f, f, 0.125, S, ql, hq, 8, maxc, part, act,
+                                        ctypes.byref(desc), None, 0, None)
+
+
+def test_int8_verify_validates_on_the_host(lib):
+    i8 = _desc(dt=B.PA_I8)
+    assert _verify8(lib, _desc(dt=B.PA_BF16)) == B.PA_ERR_INVALID      # float pool
+    assert _verify8(lib, i8, act=B.PA_F32) == B.PA_ERR_INVALID
+    assert _verify8(lib, i8, ql=0) == B.PA_ERR_INVALID
+    assert _verify8(lib, i8, ql=9) == B.PA_ERR_UNSUPPORTED              # G = 4: 36 columns
+    assert _verify8(lib, i8, ql=5, S=0) == B.PA_OK
+    # the float verify call refuses the INT8 pool
+    f = ctypes.c_void_p(FAKE)
+    assert lib.pa_verify_attention(f, f, f, f, f, f, 0.125, 4, 5, 32, 8, 100, 512, ctypes.byref(i8), None, 0,
+                                   None) == B.PA_ERR_INVALID
+    # INT8 verification splits by partitions: its workspace is the decode
+    # workspace of S x q_len rows at the same partition size
+    d8 = _desc(d=128, dt=B.PA_I8)
+    for S, ql, maxc, part in ((64, 5, 8224, 512), (3, 2, 4000, 256), (8, 8, 100, 16)):
+        assert lib.pa_verify_workspace_size(S, ql, 32, maxc, part, ctypes.byref(d8)) == \
+            lib.pa_decode_workspace_size(S * ql, 32, maxc, part, ctypes.byref(d8))
+
+
 def test_int8_without_gpu_is_a_cuda_error(lib):
     import torch
     if torch.cuda.is_available():

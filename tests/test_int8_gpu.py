@@ -254,3 +254,125 @@ def test_int8_cache_tracks_the_float_cache():
     out_q = cache.decode(wq, st)
     smax = float(cache.vs.max())
     assert float(torch.max(torch.abs(out_f.float() - out_q.float()))) <= smax + 0.05
+
+
+# ---------------------------------------------------------------------------
+# verification pass (q_len query tokens per sequence, causal) over the cache
+# ---------------------------------------------------------------------------
+
+def _verify8(wl, cache, q, ctx, part=0, max_ctx=None):
+    out = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    mc = int(ctx.max()) if max_ctx is None else max_ctx
+    pa.pa_verify_attention_int8(out, q.to(DEV), cache.kc, cache.vc, cache.ks, cache.vs,
+                                wl.decode_block_tables.contiguous().to(DEV), ctx.to(DEV), wl.scale,
+                                max_context_len=mc, partition_size=part)
+    torch.cuda.synchronize()
+    return out
+
+
+def _verify8_ref(wl, cache, q, ctx, seqs=None):
+    return oracle.verify_int8_ref(to_np(q), *cache.host, wl.decode_block_tables.contiguous().numpy(),
+                                  ctx.numpy(), wl.scale, seqs=seqs)
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,d,dtype", [
+    (32, 8, 5, 128, torch.bfloat16),    # G 4 x 5: 20 columns, three 8-column tiles
+    (32, 4, 4, 128, torch.bfloat16),    # G 8 x 4: 32 columns, four tiles
+    (8, 8, 5, 128, torch.float16),      # G 1 x 5: one tile, masked
+    (16, 8, 4, 128, torch.bfloat16),    # G 2 x 4: exactly one tile
+    (32, 8, 3, 128, torch.float16),     # G 4 x 3: two tiles, a ragged second one
+    (16, 8, 5, 64, torch.bfloat16),     # G 2 x 5: two tiles, D 64
+    (12, 4, 8, 64, torch.float16),      # G 3 x 8: three tiles, D 64
+    (32, 8, 8, 64, torch.bfloat16),     # G 4 x 8: four tiles, D 64
+])
+def test_verify_int8_shapes(hq, hkv, q_len, d, dtype):
+    wl = W.small_random(120 + hq + q_len + d, 5, 600, hq, hkv, d, dtype, kv="int8")
+    cache = Cache(wl)
+    ctx = wl.ctx0.clamp(min=q_len)
+    q = wl.verify_queries(0, q_len)
+    ref = _verify8_ref(wl, cache, q, ctx)
+    for part in (0, 16, 64, 512):
+        out = _verify8(wl, cache, q, ctx, part)
+        assert_close_to_ref(out, ref, dtype, f"int8 verify G={hq // hkv} q_len={q_len} part={part}")
+    assert pa.pa_device_status() == 0
+
+
+@pytest.mark.parametrize("ctx", [[1, 2, 4, 5, 6, 15, 16, 17, 20, 21], [31, 32, 33, 64, 65, 255, 256, 257]])
+def test_verify_int8_ragged_contexts(ctx):
+    """The causal edge at every offset of a 16-token block and at partition
+    boundaries; contexts shorter than q_len give zero rows for the queries
+    before position 0."""
+    wl = W.small_random(131, len(ctx), 0, 32, 8, 128, torch.bfloat16, ctx=ctx, kv="int8")
+    cache = Cache(wl)
+    ctx_t = torch.tensor(ctx, dtype=torch.int32)
+    q = wl.verify_queries(0, 5)
+    ref = _verify8_ref(wl, cache, q, ctx_t)
+    for part in (0, 16, 32):
+        out = _verify8(wl, cache, q, ctx_t, part)
+        assert_close_to_ref(out, ref, wl.dtype, f"int8 verify ragged part={part}")
+        for s, c in enumerate(ctx):
+            if c < 5:   # queries 0 .. 4 - c sit before position 0
+                assert int(out[s, :5 - c].count_nonzero()) == 0
+    assert pa.pa_device_status() == 0
+
+
+def test_verify_int8_q_len_1_is_decode_bit_for_bit():
+    wl = W.small_random(132, 6, 900, 32, 8, 128, torch.bfloat16, kv="int8")
+    st = wl.step(0)
+    cache = Cache(wl)
+    cache.append(st)
+    for part in (0, 64):
+        dec = cache.decode(wl, st, part)
+        ver = _verify8(wl, cache, st.q[:, None], st.context_lens, part)
+        assert torch.equal(ver[:, 0], dec)
+
+
+def test_verify_int8_last_query_is_the_decode_of_the_whole_context():
+    """Query q_len - 1 sits at position c - 1 and sees the whole context, as
+    the decode query does: with the same q row both agree within the bar."""
+    wl = W.small_random(133, 6, 900, 32, 8, 128, torch.bfloat16, kv="int8")
+    cache = Cache(wl)
+    ctx = wl.ctx0.clamp(min=5)
+    q = wl.verify_queries(0, 5)
+    ver = _verify8(wl, cache, q, ctx)
+    st = W.StepInputs(slot_mapping=torch.full((6,), -1, dtype=torch.int64), k_new=None, v_new=None,
+                      q=q[:, 4].contiguous(), context_lens=ctx)
+    dec = cache.decode(wl, st)
+    assert_close_to_ref(ver[:, 4], dec.double().cpu().numpy(), wl.dtype, "last verify query vs decode")
+
+
+def test_verify_int8_zero_contexts_and_bad_block_id():
+    wl = W.small_random(134, 4, 0, 32, 8, 128, torch.bfloat16, ctx=[40, 0, 100, 0], kv="int8")
+    cache = Cache(wl)
+    ctx = torch.tensor([40, 0, 100, 0], dtype=torch.int32)
+    q = wl.verify_queries(0, 5)
+    out = _verify8(wl, cache, q, ctx, 16)
+    assert int(out[1].count_nonzero()) == 0 and int(out[3].count_nonzero()) == 0
+    assert_close_to_ref(out, _verify8_ref(wl, cache, q, ctx), wl.dtype, "int8 verify zero contexts")
+    assert pa.pa_device_status() == 0
+    # a block id past the pool is skipped (its keys weigh nothing) and reported
+    bt = wl.decode_block_tables.contiguous().clone()
+    bt[2, 1] = wl.k_pool.shape[0] + 7
+    out2 = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    pa.pa_verify_attention_int8(out2, q.to(DEV), cache.kc, cache.vc, cache.ks, cache.vs, bt.to(DEV), ctx.to(DEV),
+                                wl.scale, max_context_len=100, partition_size=16)
+    torch.cuda.synchronize()
+    assert pa.pa_device_status() & pa.PA_DEV_BAD_BLOCK_ID
+    assert torch.equal(out2[0], out[0])       # other sequences unaffected
+
+
+def test_verify_int8_llama3_8b_full_size_sampled():
+    """The batch-64, D=128 verification of 4 drafts (q_len 5) over an INT8
+    cache in the launch configuration the benchmark times (automatic
+    partition), after the quantising append, oracle on sampled sequences."""
+    wl = W.llama3_8b_verify(steps=1, kv="int8")
+    st = wl.step(0)
+    cache = Cache(wl)
+    cache.append(st)
+    order = torch.argsort(wl.ctx0)
+    pick = sorted(set([int(order[0]), int(order[-1])] + list(range(0, 64, 9))))
+    q = wl.verify_queries(0, 5)
+    out = _verify8(wl, cache, q, st.context_lens, max_ctx=wl.max_context_len(0))
+    ref = _verify8_ref(wl, cache, q, st.context_lens, seqs=pick)
+    assert_close_to_ref(out[pick], ref[pick], wl.dtype, "int8 verify llama3-8b")
+    assert pa.pa_device_status() == 0
