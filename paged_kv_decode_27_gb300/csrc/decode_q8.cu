@@ -1,4 +1,5 @@
-// decode_q8.cu -- paged decode attention over an INT8 KV cache.
+// decode_q8.cu -- paged decode attention over an INT8 KV cache, and the
+// verification pass of speculative decoding over the same cache.
 //
 // The cache holds K and V quantised per token head ("LLM Inference Server",
 // Optional Bonus Extensions: INT8 KV-Cache Quantization; rule of its Required
@@ -38,6 +39,13 @@
 //    rescaled with the softmax's own correction, and the warp's O is
 //    multiplied by M at the end.  Positions past the context have p = 0 (their
 //    codes are finite integers and their scales are never read into p).
+//
+// Verification ("LLM Inference Server", Batched Scheduling & Speculative
+// Decoding: q_len = K + 1 query tokens per sequence) widens N: the q_len x G
+// query columns of a KV head fill NT 8-column tiles that share every widened
+// K and V fragment, and key j is masked from query i unless
+// j <= ctx - q_len + i.  Each tile holds its own accumulators, so NT > 1 runs
+// 2 CTAs per SM.
 //
 // The warps' states merge in shared memory and the split-K partials by
 // log-sum-exp exactly as in the float kernels (decode_merge.cuh).
