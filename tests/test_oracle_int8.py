@@ -134,6 +134,18 @@ def test_zero_row_and_single_nonzero():
     assert s[1] == np.float32(3.0) / np.float32(127) and c[1, 5] == -127 and np.count_nonzero(c[1]) == 1
 
 
+def test_tiny_rows_keep_the_full_code_range():
+    """No floor on the row maximum: a row whose largest magnitude is far below
+    1e-8 still maps it to +-127 (s = max / 127 in float32), and minus half of
+    it to -64 (the float32 quotient is -63.5, which rounds to the even -64)."""
+    x = np.zeros((1, 8), dtype=np.float32)
+    x[0, 0] = np.float32(2.0 ** -40)
+    x[0, 3] = np.float32(-(2.0 ** -41))
+    c, s = q8.quantize_rows_int8(x)
+    assert s[0] == np.float32(2.0 ** -40) / np.float32(127)
+    assert c[0, 0] == 127 and c[0, 3] == -64 and np.count_nonzero(c[0]) == 2
+
+
 # ---------------------------------------------------------------------------
 # append: quantise-on-write through the slot mapping
 # ---------------------------------------------------------------------------
