@@ -125,9 +125,22 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_co
                                 int partition_size, const pa_pool_desc* pool);
 
 /* The partition (tokens per split-K unit) that pa_decode_attention will use
- * for this shape: partition_size itself when nonzero, else the automatic choice. */
+ * for this shape: partition_size itself when nonzero, else the automatic
+ * choice.  The automatic choice takes the smallest partition of at least 256
+ * tokens whose (sequence, KV head, partition) units all fit one resident wave
+ * of the current device (3 decode CTAs per SM, the SM count queried from the
+ * device); when even 2048-token partitions overflow a wave it takes 1024.
+ * With no device current (planning on a host without a GPU) it assumes a full
+ * GB300's 152 SMs.  pa_decode_workspace_size follows the same choice, so
+ * size the workspace with the device that will run the call current. */
 PA_API int pa_decode_partition_size(int num_seqs, int max_context_len, int partition_size,
                              const pa_pool_desc* pool);
+
+/* The automatic choice above for a device of sm_count SMs (e.g. to plan for a
+ * partition of a GPU).  Returns 0 and sets pa_last_error on invalid arguments
+ * (sm_count < 1, a bad pool). */
+PA_API int pa_decode_partition_size_on(int num_seqs, int max_context_len, int partition_size,
+                                       const pa_pool_desc* pool, int sm_count);
 
 /*
  * pa_decode_attention -- one query token per sequence over its paged cache.
@@ -475,7 +488,9 @@ PA_API int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int 
  *    before anything is enqueued.  A larger partition_size needs less.
  *  - The first call on a device that needs the array looks up its device
  *    address (cudaGetSymbolAddress) with that device current; make that first
- *    call before any stream capture.
+ *    call before any stream capture.  The address is remembered with the
+ *    CUDA context it belongs to: after a device reset the next call looks it
+ *    up again (so that call, too, should come before any capture).
  *  - Every call on a device shares the array and it keeps the last call's
  *    contents.  The split-K completion counters at its start must be zero
  *    when a call begins: each call clears the ones it uses (an asynchronous

@@ -67,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, pdesc]
     L.pa_decode_partition_size.restype = i32
     L.pa_decode_partition_size.argtypes = [i32, i32, i32, pdesc]
+    L.pa_decode_partition_size_on.restype = i32
+    L.pa_decode_partition_size_on.argtypes = [i32, i32, i32, pdesc, i32]
     L.pa_decode_attention.restype = i32
     L.pa_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, pdesc,
                                       vp, sz, vp]
@@ -205,6 +207,18 @@ def pa_decode_partition_size(num_seqs: int, max_context_len: int, k_pool: torch.
     desc = pool_desc(k_pool)
     return int(L.pa_decode_partition_size(int(num_seqs), int(max_context_len), int(partition_size),
                                           ctypes.byref(desc)))
+
+
+def pa_decode_partition_size_on(num_seqs: int, max_context_len: int, k_pool: torch.Tensor, sm_count: int,
+                                partition_size: int = 0) -> int:
+    """The automatic partition choice for a device of ``sm_count`` SMs."""
+    L = load_library()
+    desc = pool_desc(k_pool)
+    n = int(L.pa_decode_partition_size_on(int(num_seqs), int(max_context_len), int(partition_size),
+                                          ctypes.byref(desc), int(sm_count)))
+    if n == 0:
+        raise PaError(PA_ERR_INVALID, pa_last_error())
+    return n
 
 
 def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

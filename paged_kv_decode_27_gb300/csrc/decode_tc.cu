@@ -227,16 +227,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       mu[0] = nu0;
       mu[1] = nu1;
     }
-    const float p0 = fast_exp2(x0 - mu[0]);
-    const float p1 = fast_exp2(x1 - mu[1]);
-    const float p2 = fast_exp2(x2 - mu[0]);
-    const float p3 = fast_exp2(x3 - mu[1]);
-    l_run[0] += p0 + p2;
-    l_run[1] += p1 + p3;
+    // The weights enter the PV product rounded to T; the normaliser sums the
+    // same rounded values, so numerator and denominator use identical weights.
+    const uint32_t pk0 = Mma<T>::pack(fast_exp2(x0 - mu[0]), fast_exp2(x1 - mu[1]));   // token g
+    const uint32_t pk1 = Mma<T>::pack(fast_exp2(x2 - mu[0]), fast_exp2(x3 - mu[1]));   // token g + 8
+    const float2 r0 = Mma<T>::unpack(pk0);
+    const float2 r1 = Mma<T>::unpack(pk1);
+    l_run[0] += r0.x + r1.x;
+    l_run[1] += r0.y + r1.y;
 
     // P^T as the B operand (k = token, n = head): transpose the two 8x8 halves
-    const uint32_t pb0 = movmatrix_trans(Mma<T>::pack(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(Mma<T>::pack(p2, p3));
+    const uint32_t pb0 = movmatrix_trans(pk0);
+    const uint32_t pb1 = movmatrix_trans(pk1);
 
     // ---- O^T[d][head] += V^T[d][token] P^T[token][head] --------------------
     const bool partial = nvalid < kBlock;

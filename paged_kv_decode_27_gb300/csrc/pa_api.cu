@@ -22,10 +22,13 @@ __device__ int g_pa_status = 0;
 
 namespace {
 
-constexpr int kGb300Sms = 152;
-// Decode CTAs resident at once (3 per SM), and the smallest partition the
-// automatic choice uses: below it the split-K merge costs more than it hides.
-constexpr long long kWaveUnits = 3LL * kGb300Sms;
+// SMs assumed by the sizing calls when no device is current (a full GB300,
+// the part sm_103a code runs on); with a device current its own count is used.
+constexpr int kDefaultSms = 152;
+// Decode CTAs resident on one SM at once (three 64 KB stage sets), and the
+// smallest partition the automatic choice uses: below it the split-K merge
+// costs more than it hides.
+constexpr int kCtasPerSm = 3;
 constexpr int kMinPartition = 256;
 constexpr int kMaxPartition = 2048;   // 32 blocks per warp of a 4-warp CTA
 // Split-K completion counters occupy a fixed region at the start of the
@@ -92,30 +95,45 @@ int check_pool(const pa_pool_desc* pool) {
 int* status_ptr() {
   static std::mutex mu;
   static int* cache[64] = {};
+  static void* cache_ctx[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
+  if (!cache[dev] || cache_ctx[dev] != pa::current_context()) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return nullptr;
     cache[dev] = static_cast<int*>(p);
+    // the lookup made the device's primary context current if none was
+    cache_ctx[dev] = pa::current_context();
   }
   return cache[dev];
 }
 
-int choose_partition(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
+// SMs of the current device, or kDefaultSms when none is current.
+int current_sms() {
+  const int n = pa::device_sm_count();
+  return n > 0 ? n : kDefaultSms;
+}
+
+int choose_partition_on(int num_seqs, int num_kv_heads, int max_context_len, int requested, int sms) {
   if (requested > 0) return requested;
   // One resident wave when the batch allows it: the largest partition count
   // (smallest partition, not below kMinPartition) whose (sequence, KV head,
   // partition) units all fit on the GPU at once.  Past that the decode runs in
   // several waves of 1024-token partitions.
+  const long long wave = static_cast<long long>(kCtasPerSm) * (sms > 0 ? sms : kDefaultSms);
   const auto units = [&](int p) {
     return static_cast<long long>(num_seqs) * num_kv_heads * ((max_context_len + p - 1) / p);
   };
-  if (units(kMaxPartition) > kWaveUnits) return 1024;
+  if (units(kMaxPartition) > wave) return 1024;
   int p = kMaxPartition;
-  while (p > kMinPartition && units(p / 2) <= kWaveUnits) p /= 2;
+  while (p > kMinPartition && units(p / 2) <= wave) p /= 2;
   return p;
+}
+
+int choose_partition(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
+  return choose_partition_on(num_seqs, num_kv_heads, max_context_len, requested,
+                             requested > 0 ? kDefaultSms : current_sms());
 }
 
 int max_splits_for(int max_context_len, int part_blocks) {
@@ -256,6 +274,35 @@ int set_last_error(int code, const char* msg) {
   t_err = msg;
   return code;
 }
+
+void* current_context() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  static GetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<GetCurrent>(nullptr);
+    return reinterpret_cast<GetCurrent>(p);
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
 }  // namespace pa
 
 extern "C" {
@@ -293,6 +340,17 @@ int pa_decode_partition_size(int num_seqs, int max_context_len, int partition_si
   t_err.clear();
   if (check_pool(pool) != PA_OK) return 0;
   return choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+}
+
+int pa_decode_partition_size_on(int num_seqs, int max_context_len, int partition_size,
+                                const pa_pool_desc* pool, int sm_count) {
+  t_err.clear();
+  if (check_pool(pool) != PA_OK) return 0;
+  if (sm_count < 1) {
+    fail(PA_ERR_INVALID, "sm_count must be >= 1");
+    return 0;
+  }
+  return choose_partition_on(num_seqs, pool->num_kv_heads, max_context_len, partition_size, sm_count);
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int max_context_len, int partition_size,

@@ -60,6 +60,16 @@ struct PrefillArgs {
 // Record `msg` as the calling thread's pa_last_error() and return `code`.
 int set_last_error(int code, const char* msg);
 
+// The calling thread's current CUDA context (driver handle), or null.  Device
+// addresses of the library's __device__ variables are cached per (device,
+// context): a device reset creates a new context, whose module may place them
+// elsewhere, so a changed handle triggers a fresh lookup.
+void* current_context();
+
+// Streaming multiprocessors of the current device (queried once per device;
+// 0 when no device is current).
+int device_sm_count();
+
 cudaError_t launch_append(void* k_pool, void* v_pool, const int64_t* slot_mapping,
                           const void* k_new, const void* v_new, int num_tokens,
                           int num_kv_heads, int row_bytes, int num_blocks, int* status,

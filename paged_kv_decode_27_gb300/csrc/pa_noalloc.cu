@@ -31,10 +31,13 @@ namespace {
 // Device address of the array for the current device.  Looked up once per
 // device, with that device current, on the first call that needs it: in host
 // code the array's name is only a host-side stand-in, so the real address must
-// come from cudaGetSymbolAddress.
+// come from cudaGetSymbolAddress.  The address is kept together with the
+// context it was found in; after a device reset (a new context, whose module
+// may sit elsewhere) the next call looks it up again.
 void* noalloc_scratch(cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static void* addr_ctx[64] = {};
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
@@ -43,11 +46,12 @@ void* noalloc_scratch(cudaError_t* err) {
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || addr_ctx[dev] != pa::current_context()) {
     void* p = nullptr;
     *err = cudaGetSymbolAddress(&p, g_pa_noalloc_scratch);
     if (*err != cudaSuccess) return nullptr;
     addr[dev] = p;
+    addr_ctx[dev] = pa::current_context();
   }
   return addr[dev];
 }

@@ -125,6 +125,29 @@ def test_workspace_size_and_partition(lib):
     assert lib.pa_decode_partition_size(4, 512, 256, ctypes.byref(d)) == 256
 
 
+def test_partition_choice_follows_the_sm_count(lib):
+    """The automatic partition is sized to one resident wave of 3 CTAs per SM
+    of the device it is asked for, not to a fixed SM count."""
+    lib.pa_decode_partition_size_on.restype = ctypes.c_int
+    lib.pa_decode_partition_size_on.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(B.pa_pool_desc), ctypes.c_int]
+    d = _desc(d=128)
+    on = lambda S, maxc, sms, part=0, desc=d: lib.pa_decode_partition_size_on(S, maxc, part, ctypes.byref(desc), sms)
+    # 8 x 8 pairs of 8192 tokens: 64 pairs x 4 partitions of 2048 = 256 units.
+    # 152 SMs (456 slots): 2048 (1024 would need 512 units)
+    assert on(8, 8192, 152) == 2048
+    # 176 SMs (528 slots): 1024 fits; 352 SMs (1056): 512 fits (1024 units)
+    assert on(8, 8192, 176) == 1024 and on(8, 8192, 352) == 512
+    # 64 SMs (192 slots): not even 2048-token partitions fit one wave -> 1024, several waves
+    assert on(8, 8192, 64) == 1024
+    # every choice stays in [256, 2048]
+    for sms in (1, 8, 76, 132, 152, 160, 1000, 100000):
+        p = on(3, 3000, sms)
+        assert 256 <= p <= 2048 and p % 16 == 0
+    # a forced partition is returned as is; a bad SM count is refused
+    assert on(8, 8192, 64, part=128) == 128
+    assert on(8, 8192, 0) == 0 and lib.pa_last_error()
+
+
 def test_no_gpu_means_cuda_error_not_a_crash(lib):
     import torch
     if torch.cuda.is_available():

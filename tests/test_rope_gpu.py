@@ -1,15 +1,24 @@
 """RoPE fused into the append, on the GPU, against the float64 oracle.
 
+Every expected value here is computed from oracle inputs alone: the oracle
+builds its own (cos, sin) table (``oracle.rope_cache_ref``) and never sees the
+table the GPU built.
+
 Bars, from the arithmetic:
   * table: float64 angle and trigonometry on both sides, rounded once to
     float32: |gpu - ref| <= 1 ulp of float32 at |ref| plus the float64 error of
     the angle itself (pow is within 2 ulp on either side, so the angle p * f
     may differ by 4 * 2^-52 * p * f, which moves cos / sin by as much in
     absolute terms -- visible only next to their zeros);
-  * rotation: fp32 a*c - b*s with one fused multiply-add, then one rounding to
-    the element type, against the exact float64 rotation on the same table:
-    |gpu - ref| <= half an ulp of the element type at |ref| plus
-    2^-22 (|a| + |b|) for the fp32 arithmetic;
+  * rotation: the GPU computes fp32 a*c - b*s (one fused multiply-add) on ITS
+    table, then rounds once to the element type; the oracle rotates exactly
+    in float64 on the oracle's table.  The two tables differ by at most the
+    table bar above, |dc|, |ds| <= 2^-23 + 4 * 2^-52 * p * f (cos and sin lie
+    in [-1, 1], where a float32 ulp is at most 2^-23), which moves the exact
+    rotation by at most that much times (|a| + |b|).  So
+    |gpu - ref| <= e + half an ulp of the element type at |ref| + e, with
+    e = (2^-22 + 2^-23 + 4 * 2^-52 * p * f_max) (|a| + |b|), the first term
+    being the fp32 arithmetic;
   * V rows: bit-exact copies, untouched slots untouched.
 """
 from __future__ import annotations
@@ -34,14 +43,18 @@ def gpu_cache(max_pos, d, theta):
     return cs
 
 
-def rotation_bound(x: torch.Tensor, ref: np.ndarray) -> np.ndarray:
-    """half an ulp of the element type at |ref| + 2^-22 (|a| + |b|) per pair."""
+def rotation_bound(x: torch.Tensor, ref: np.ndarray, max_angle: float) -> np.ndarray:
+    """e + half an ulp of the element type at |ref| + e, with
+    e = (2^-22 + 2^-23 + 4 * 2^-52 * max_angle) (|a| + |b|) per pair: the fp32
+    arithmetic plus the largest difference between the GPU's table and the
+    oracle's (max_angle bounds p * f over the rows checked)."""
     a = np.abs(to_f64(x))
     h = a.shape[-1] // 2
     pair = np.concatenate([a[..., :h] + a[..., h:]] * 2, axis=-1)
+    e = (2.0 ** -22 + 2.0 ** -23 + 4 * 2.0 ** -52 * max_angle) * pair
     mant = {torch.float32: 23, torch.bfloat16: 7, torch.float16: 10}[x.dtype]
-    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - mant)
-    return 0.5 * ulp + 2.0 ** -22 * pair + 1e-30
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref) + e, 1e-30))) - mant)
+    return e + 0.5 * ulp + 1e-30
 
 
 @pytest.mark.parametrize("d,theta", [(128, 10000.0), (128, 500000.0), (64, 10000.0)])
@@ -75,7 +88,7 @@ def test_append_rope_rotates_k_and_copies_v(dtype, d):
     torch.cuda.synchronize()
     assert pa.pa_device_status() == 0
     k_rot, v_ref = oracle.append_rope_ref(to_np(vp), slots.numpy(), pos.numpy(), to_np(k_new), to_np(v_new),
-                                          cs.cpu().numpy())
+                                          oracle.rope_cache_ref(8192, d, 10000.0))
     assert np.array_equal(to_np(vd).view(np.uint8), v_ref.view(np.uint8))
     kg = kd.cpu()
     written = torch.zeros((nb, 16), dtype=torch.bool)
@@ -87,7 +100,7 @@ def test_append_rope_rotates_k_and_copies_v(dtype, d):
         written[b, o] = True
         got = to_f64(kg[b, :, o])
         err = np.abs(got - k_rot[t])
-        assert np.all(err <= rotation_bound(k_new[t], k_rot[t])), (t, float(err.max()))
+        assert np.all(err <= rotation_bound(k_new[t], k_rot[t], float(pos[t]))), (t, float(err.max()))
     # position 0 is the identity: that row is copied exactly
     b0, o0 = divmod(int(slots[0]), 16)
     assert torch.equal(kg[b0, :, o0], k_new[0])
@@ -105,8 +118,8 @@ def test_apply_rope_in_place(dtype):
     xd = x.to(DEV)
     pa.pa_apply_rope(xd, pos.to(DEV), cs)
     torch.cuda.synchronize()
-    ref = oracle.rope_rotate_ref(to_np(x), pos.numpy(), cs.cpu().numpy())
-    assert np.all(np.abs(to_f64(xd) - ref) <= rotation_bound(x, ref))
+    ref = oracle.rope_rotate_ref(to_np(x), pos.numpy(), oracle.rope_cache_ref(4096, d, 500000.0))
+    assert np.all(np.abs(to_f64(xd) - ref) <= rotation_bound(x, ref, 4095.0))
 
 
 def test_bad_position_is_skipped_and_reported():
@@ -148,8 +161,8 @@ def test_decode_over_rotated_cache_matches_oracle_and_depends_on_relative_positi
     wl = W.small_random(141, 4, 0, 16, 4, 128, torch.bfloat16, ctx=[17, 100, 333, 64])
     cs = gpu_cache(8192, 128, 10000.0)
     out0, (slots, pos, kn, vn, q, kp, vp) = _rope_decode(wl, 0, cs)
-    # oracle: rotate in float64 with the same table, decode over the rotated cache
-    csn = cs.cpu().numpy()
+    # oracle: its own table, rotation in float64, decode over the rotated cache
+    csn = oracle.rope_cache_ref(8192, 128, 10000.0)
     k_rot = oracle.rope_rotate_ref(to_np(kn), pos.numpy(), csn)
     q_rot = oracle.rope_rotate_ref(to_np(q), (wl.ctx0 - 1).numpy(), csn)
     k_pool = oracle.as_f64(to_np(wl.k_pool)).copy()

@@ -30,8 +30,9 @@ def lib():
 def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row(lib):
     """Two consecutive calls (different shapes, both split-K so the built-in
     array is really used, the second after the first left its partials there)
-    agree with pa_decode_attention given a caller workspace, within the bf16
-    parity bar."""
+    agree with pa_decode_attention given a caller workspace.  Both run the
+    same kernel with the same partition and merge order, so the outputs must
+    be bit-identical (which is also within the bf16 parity bar)."""
     dev = "cuda"
     cases = [W.small_random(90, 8, 3000, 32, 8, 128, torch.bfloat16),
              W.small_random(91, 5, 1500, 16, 4, 64, torch.bfloat16)]
@@ -50,20 +51,25 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row(lib):
         torch.cuda.synchronize()
         err = (out.float() - ref.float()).abs()
         assert bool((err <= atol + rtol * ref.float().abs()).all()), f"max err {err.max().item():.3e}"
+        assert torch.equal(out, ref)
     assert pa.pa_device_status() == 0
 
 
 def test_noalloc_rejects_shapes_beyond_the_array(lib):
-    """64 sequences x 32 heads at 64k tokens need ~135 MB of partials: refused
-    on the host with a clear message, before any device work (the pointers
-    below are never dereferenced)."""
-    fake = ctypes.c_void_p(0x10000000)
+    """64 sequences x 32 heads at 64k tokens (1024-token partitions, 64 splits)
+    need about 67 MB of partials (64 x 32 x 64 rows of 128 fp32 values):
+    refused on the host with a clear message, before any device work.  out and
+    q are NULL, so even a call that got past the size check would be refused
+    as a null-pointer error and never launch."""
     desc = pa.pa_pool_desc(4096 * 8, 8, 16, 128, pa.PA_BF16)
+    lib.pa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.pa_decode_workspace_size.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(pa.pa_pool_desc)]
+    assert lib.pa_decode_workspace_size(64, 32, 65536, 0, ctypes.byref(desc)) > pa.PA_NOALLOC_SCRATCH_BYTES
     fn = lib.pa_decode_attention_noalloc
     fn.restype = ctypes.c_int
     fn.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_float] + [ctypes.c_int] * 5 + \
         [ctypes.POINTER(pa.pa_pool_desc), ctypes.c_void_p]
-    rc = fn(fake, fake, fake, fake, fake, fake, 0.08, 64, 32, 4096, 65536, 0, ctypes.byref(desc), None)
+    rc = fn(None, None, None, None, None, None, 0.08, 64, 32, 4096, 65536, 0, ctypes.byref(desc), None)
     assert rc == pa.PA_ERR_INVALID
     msg = pa.pa_last_error()
     assert "scratch" in msg and str(pa.PA_NOALLOC_SCRATCH_BYTES) in msg
