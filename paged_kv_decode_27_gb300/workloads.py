@@ -334,6 +334,20 @@ def llama3_8b_decode(steps: int = 32, batch: int = 64, kv: str = "float") -> Wor
                        (", INT8 KV cache" if kv == "int8" else ""))
 
 
+def llama3_8b_long(batch: int, steps: int = 32) -> Workload:
+    """The Llama-3-8B head shape (h_q=32, h_kv=8, D=128, bf16) at the
+    small-batch end of the decode range: ``batch`` sequences (1 or 4 in the
+    tests and the benchmark) whose contexts reach 8192 on the last step
+    (8192 - steps + 1 at step 0), blocks randomly permuted in a pool of 1.25x
+    the need, values N(0, 1).  The batch is the speculative-decoding setting
+    of "Mini inference engine", section 7 (batch 1)."""
+    cid = 30 + batch
+    ctx0 = torch.full((batch,), 8192 - steps + 1, dtype=torch.int64)
+    return _multi_step(cid, "llama3_8b_long_b%d" % batch, batch, 32, 8, 128, steps, ctx0, 1.0,
+                       description="Llama-3-8B-shaped long-context decode, bf16, batch %d, "
+                                   "contexts up to 8192" % batch)
+
+
 def prefix_shared_8k() -> Workload:
     """8 sequences of context 8192 whose first 13 blocks (208 tokens, a shared
     system prompt) are the same physical blocks; h_q=32, h_kv=8, D=128, bf16."""
@@ -386,6 +400,8 @@ WORKLOADS = {
     "llama3_8b_verify": lambda: llama3_8b_verify(),
     "llama3_8b_verify_int8": lambda: llama3_8b_verify(kv="int8"),
     "llama3_8b_decode_rope": lambda: llama3_8b_decode_rope(),
+    "llama3_8b_long_b1": lambda: llama3_8b_long(1),
+    "llama3_8b_long_b4": lambda: llama3_8b_long(4),
 }
 
 

@@ -45,22 +45,32 @@ def test_llama32_1b_steps():
         kp, vp, k_np, v_np = _step_and_check(wl, t, (0, 256), kp=kp, vp=vp, k_np=k_np, v_np=v_np)
 
 
-def test_llama3_8b_full_size_sampled():
+def test_llama3_8b_full_size():
     """The batch-64, D=128 workload in the launch configuration the benchmark
-    times (automatic partition), oracle on 12 sampled sequences including the
-    shortest and the longest."""
+    times (automatic partition): every output row of two consecutive steps
+    against the oracle."""
     wl = W.llama3_8b_decode(steps=2)
-    ctx = wl.ctx0
-    order = torch.argsort(ctx)
-    pick = sorted(set([int(order[0]), int(order[-1])] + list(range(0, 64, 6))))
     kp = vp = k_np = v_np = None
     for t in range(2):
-        kp, vp, k_np, v_np = _step_and_check(wl, t, (0,), seqs=pick, kp=kp, vp=vp, k_np=k_np, v_np=v_np)
+        kp, vp, k_np, v_np = _step_and_check(wl, t, (0,), kp=kp, vp=vp, k_np=k_np, v_np=v_np)
 
 
 def test_prefix_shared_8k_split_k():
+    """All 8 sequences of 8192 tokens (13 shared blocks), automatic, 2048- and
+    64-token partitions (4 and 128 partials merged per row)."""
     wl = W.prefix_shared_8k()
-    _step_and_check(wl, 0, (0, 2048, 64), seqs=[0, 3, 7])
+    _step_and_check(wl, 0, (0, 2048, 64))
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_llama3_8b_long_context_small_batch(batch):
+    """Batch 1 and batch 4 at contexts near 8192 (the small-batch end of the
+    decode range, where split-K carries all the parallelism): every row, two
+    steps, the automatic partition and two forced ones."""
+    wl = W.llama3_8b_long(batch, steps=2)
+    kp = vp = k_np = v_np = None
+    for t in range(2):
+        kp, vp, k_np, v_np = _step_and_check(wl, t, (0, 128, 2048), kp=kp, vp=vp, k_np=k_np, v_np=v_np)
 
 
 def test_prefix_shared_identical_tails_give_identical_outputs():
@@ -84,8 +94,9 @@ def test_prefix_shared_identical_tails_give_identical_outputs():
 
 
 def test_mixed_step_decode_part():
+    """The 60 decode sequences of the mixed continuous-batching step, every row."""
     wl = W.mixed_mistral7b()
-    _step_and_check(wl, 0, (0,), seqs=list(range(0, 60, 5)))
+    _step_and_check(wl, 0, (0,))
 
 
 @pytest.mark.parametrize("ctx", [[1, 15, 16, 17, 31, 32, 33], [63, 64, 65, 127, 128, 129, 255, 256, 257]])

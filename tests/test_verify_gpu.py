@@ -122,17 +122,15 @@ def test_verify_short_contexts_give_zero_leading_rows():
     assert_close_to_ref(out, _ref(wl, q, ctx), wl.dtype, "short contexts")
 
 
-def test_verify_llama3_8b_full_size_sampled():
+def test_verify_llama3_8b_full_size():
     """Batch 64, D 128, K = 4 drafts (q_len 5) in the benchmark's launch
-    configuration (automatic partition); oracle on sampled sequences."""
+    configuration (automatic partition): every row against the oracle."""
     wl = W.llama3_8b_decode(steps=1)
     ctx = wl.ctx0
     q = wl.verify_queries(0, 5)
-    order = torch.argsort(ctx)
-    pick = sorted(set([int(order[0]), int(order[-1])] + list(range(0, 64, 9))))
     out = _verify(wl, q, ctx)
-    ref = _ref(wl, q, ctx, seqs=pick)
-    assert_close_to_ref(out[pick], ref[pick], wl.dtype, "verify llama3-8b")
+    ref = _ref(wl, q, ctx)
+    assert_close_to_ref(out, ref, wl.dtype, "verify llama3-8b")
     assert pa.pa_device_status() == 0
 
 
@@ -160,10 +158,9 @@ def test_verify_many_segments_per_cta(part):
     wl = W.small_random(103, len(ctx_l), 0, 32, 8, 128, torch.bfloat16, ctx=ctx_l)
     ctx = torch.tensor(ctx_l, dtype=torch.int32).clamp(min=5)
     q = wl.verify_queries(0, 5)
-    pick = list(range(0, 90, 7)) + [88, 89]
     out = _verify(wl, q, ctx, part)
-    ref = _ref(wl, q, ctx, seqs=pick)
-    assert_close_to_ref(out[pick], ref[pick], wl.dtype, f"many segments part={part}")
+    ref = _ref(wl, q, ctx)
+    assert_close_to_ref(out, ref, wl.dtype, f"many segments part={part}")
     assert pa.pa_device_status() == 0
 
 
