@@ -212,6 +212,86 @@ print(json.dumps({"seconds": el, "steps": steps, "bytes": b, "tokens": tok}))
             "seconds": rec["seconds"]}
 
 
+def cpu_oracle_more(max_seconds: float = 6.0):
+    """The float64 oracle on the host cores, beyond the 1-thread headline
+    figure: (1) the same headline decode steps spread over every core the
+    process may use (one single-threaded worker process per core, each taking
+    whole sequences), wall clock; (2) one decode step of every benchmark
+    configuration on one thread (the mixed step's prompt pass on its
+    512-token prompt only).  Runs in a fresh process with no GPU."""
+    code = r"""
+import json, os, sys, time
+sys.path.insert(0, %r)
+import numpy as np
+import torch
+torch.set_num_threads(1)
+import multiprocessing as mp
+import oracle
+from paged_kv_decode_27_gb300 import workloads as W
+def npv(t):
+    t = t.contiguous()
+    return t.view(torch.int16).numpy().view('uint16') if t.dtype == torch.bfloat16 else t.numpy()
+cores = len(os.sched_getaffinity(0))
+res = {"cores": cores}
+# (1) headline steps 0..n-1 on all cores: the pool after the appends of steps 0..n-1 serves
+# every one of those steps (a step reads only positions below its own contexts)
+wl = W.llama3_8b_decode()
+kp, vp = npv(wl.k_pool), npv(wl.v_pool)
+n = 4
+sts = [wl.step(t) for t in range(n)]
+for st in sts:
+    kp, vp = oracle.append_ref(kp, vp, st.slot_mapping.numpy(), npv(st.k_new), npv(st.v_new))
+bt = wl.decode_block_tables.contiguous().numpy()
+QS = [npv(st.q) for st in sts]
+CT = [st.context_lens.numpy() for st in sts]
+jobs = [(t, s) for t in range(n) for s in range(64)]
+def work(part):
+    for t, s in part:
+        oracle.decode_ref(QS[t], kp, vp, bt, CT[t], wl.scale, seqs=[s])
+    return len(part)
+# workers are forked here, in a process that never touched a GPU
+ctx = mp.get_context("fork")
+parts = [jobs[i::cores] for i in range(cores)]
+with ctx.Pool(cores) as pool:
+    pool.map(work, [parts[0][:1]] * cores)      # start-up, untimed
+    t0 = time.perf_counter()
+    pool.map(work, parts)
+    el = time.perf_counter() - t0
+b = sum(int(c) * 2 * 8 * 128 * 2 + 2 * 32 * 128 * 2 + 4 * ((int(c) + 15) // 16) + 4 for ct in CT for c in ct)
+res["all_cores"] = {"value": b / el / 1e9, "unit": "GB/s", "cores": cores, "seconds": el,
+                    "sample": f"decode steps 0..{n-1} of llama3_8b_decode in full (64 sequences x 32 q heads), "
+                              f"one single-threaded worker process per core, whole sequences per task"}
+# (2) one step of every configuration, one thread
+per = {}
+for name in %r:
+    w = wl if name == wl.name else W.WORKLOADS[name]()
+    st = w.step(0)
+    k2, v2 = oracle.append_ref(npv(w.k_pool), npv(w.v_pool), st.slot_mapping.numpy(), npv(st.k_new), npv(st.v_new))
+    t0 = time.perf_counter()
+    oracle.decode_ref(npv(st.q), k2, v2, w.decode_block_tables.contiguous().numpy(), st.context_lens.numpy(), w.scale)
+    rec = {"decode_s": time.perf_counter() - t0, "decode_bytes": w.decode_bytes(0)}
+    if w.prompt_lens:
+        rows = list(range(int(st.cu_q_lens[0]), int(st.cu_q_lens[1])))
+        t0 = time.perf_counter()
+        oracle.prefill_ref(npv(st.q_prefill), k2, v2, w.prefill_block_tables.contiguous().numpy(),
+                           st.cu_q_lens.numpy(), st.prefill_context_lens.numpy(), w.scale, rows=rows)
+        rec["prefill_first_prompt_s"] = time.perf_counter() - t0
+        rec["prefill_first_prompt_tokens"] = len(rows)
+    per[name] = rec
+res["per_config_1_thread"] = per
+print(json.dumps(res))
+""" % (ROOT, [c for c in CONFIGS])
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    except Exception as exc:
+        return {"failed": type(exc).__name__}
+    if r.returncode != 0:
+        return {"failed": (r.stderr.strip().splitlines() or ["no output"])[-1]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle, timed on the host cores
 # ---------------------------------------------------------------------------
@@ -277,10 +357,15 @@ def run_ours(args, rank, world, local_rank):
     from paged_kv_decode_27_gb300 import binding as pa
     from paged_kv_decode_27_gb300 import workloads as W
 
-    # the CPU oracle baseline runs first, in its own 1-thread process
+    # the CPU oracle baseline runs first, in its own 1-thread process, then on all cores
     cpu = None
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         cpu = cpu_baseline()
+        if world == 1:
+            more = cpu_oracle_more()
+            cpu["host_cores"] = more.get("cores", len(os.sched_getaffinity(0)))
+            cpu["all_cores"] = more.get("all_cores", more)
+            cpu["per_config_1_thread"] = more.get("per_config_1_thread")
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -488,6 +573,12 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     clocks = sampler.summary(t_busy0, t_wall1 + 0.1) if sampler else None
+    # every configuration of the workload list, per call (L2 evicted), after the timed region
+    configs = None
+    if world == 1 and not args.quick:
+        del kp, vp, dev_in, p_bufs, p_views, graphs
+        torch.cuda.empty_cache()
+        configs = measure_configs(pa, W, torch, dev)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -514,6 +605,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "device_status": status,
         "cpu_baseline": cpu,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 
@@ -522,20 +614,39 @@ def run_ours(args, rank, world, local_rank):
 # per-call figures of the other workloads
 # ---------------------------------------------------------------------------
 
-def run_other(args):
-    """Append / prefill / decode times of one workload, each call bracketed by
-    CUDA events on its stream, with L2 evicted (a 512 MB read) before every
-    step so that each call reads its inputs from HBM."""
-    import torch
+# Layers of the model each workload's head shape comes from (attention-only
+# per-model figures divide the one-layer rate by this).
+N_LAYERS = {"tiny_fp32": 1, "llama32_1b_decode": 16, "llama3_8b_decode": 32, "prefix_shared_8k": 32,
+            "mixed_mistral7b": 32, "llama3_8b_long_b1": 32, "llama3_8b_long_b4": 32}
+# The five configurations of the benchmark's workload list, then the small-batch
+# end of its decode range (batch 1 and 4 at contexts up to 8192).
+CONFIGS = ["tiny_fp32", "llama32_1b_decode", "llama3_8b_decode", "prefix_shared_8k", "mixed_mistral7b",
+           "llama3_8b_long_b1", "llama3_8b_long_b4"]
 
-    import __graft_entry__
-    __graft_entry__.build()
-    from paged_kv_decode_27_gb300 import binding as pa
-    from paged_kv_decode_27_gb300 import workloads as W
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    wl = W.WORKLOADS[args.workload]()
+def peak_bf16():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def l2_flusher(torch, dev):
+    """A read of twice the L2 size (L2 from the device attribute), which
+    evicts every line without leaving dirty ones behind (a write would make the
+    timed call pay for their write-back)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (129 << 20)
+    buf = torch.ones(max(2 * l2, 256 << 20) // 2, dtype=torch.float16, device=dev)
+    return lambda: buf.sum()
+
+
+def measure_workload(name, pa, W, torch, dev, reps, warmup, partition=0, flush=None):
+    """Append / prefill / attention times of one workload, each call bracketed by
+    CUDA events on its stream, with L2 evicted before every repetition so that
+    each call reads its inputs from HBM.  Median and p90 over `reps` calls."""
+    wl = W.WORKLOADS[name]()
     kp, vp = wl.k_pool.to(dev), wl.v_pool.to(dev)
     ks = wl.k_scales.to(dev) if wl.kv_int8 else None
     vs = wl.v_scales.to(dev) if wl.kv_int8 else None
@@ -552,7 +663,7 @@ def run_other(args):
         d_in.append(d)
     max_ctx = wl.max_context_len(wl.steps - 1)
     S, hq, dh = wl.num_decode_seqs, wl.num_q_heads, wl.head_dim
-    ws = torch.zeros(max(1, pa.pa_decode_workspace_size(S, hq, max_ctx, kp, args.partition)),
+    ws = torch.zeros(max(1, pa.pa_decode_workspace_size(S, hq, max_ctx, kp, partition)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((S, hq, dh), dtype=wl.dtype, device=dev)
     vq = wl.extra.get("verify_q_len", 0)
@@ -560,7 +671,7 @@ def run_other(args):
         for t, d in enumerate(d_in):
             d["vq"] = wl.verify_queries(t, vq).to(dev)
         out = torch.empty((S, vq, hq, dh), dtype=wl.dtype, device=dev)
-        ws = torch.zeros(max(1, pa.pa_verify_workspace_size(S, vq, hq, max_ctx, kp, args.partition)),
+        ws = torch.zeros(max(1, pa.pa_verify_workspace_size(S, vq, hq, max_ctx, kp, partition)),
                          dtype=torch.uint8, device=dev)
     theta = wl.extra.get("rope_theta")
     if theta:   # RoPE: K rotated on the append, q rotated at position context - 1
@@ -569,14 +680,14 @@ def run_other(args):
         for d in d_in:
             d["pos"] = (d["ctx"] - 1).to(torch.int32)
             d["q0"] = d["q"].clone()
-    flush = torch.ones(256 << 20, dtype=torch.float16, device=dev)   # 512 MB, read to evict L2
+    flush = flush or l2_flusher(torch, dev)
     stream = torch.cuda.current_stream()
     rec = {"append": [], "prefill": [], "decode": []}
 
     def step(t, timed):
         d = d_in[t % wl.steps]
         if timed:
-            flush.sum()   # reads 512 MB: evicts L2 without leaving dirty lines behind
+            flush()
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         if theta:
             d["q"].copy_(d["q0"])   # the queries arrive unrotated every step
@@ -596,52 +707,133 @@ def run_other(args):
         evs[2].record(stream)
         if vq and wl.kv_int8:
             pa.pa_verify_attention_int8(out, d["vq"], kp, vp, ks, vs, bt, d["ctx"], wl.scale,
-                                        max_context_len=max_ctx, partition_size=args.partition, workspace=ws,
+                                        max_context_len=max_ctx, partition_size=partition, workspace=ws,
                                         stream=stream)
         elif vq:
             pa.pa_verify_attention(out, d["vq"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
-                                   partition_size=args.partition, workspace=ws, stream=stream)
+                                   partition_size=partition, workspace=ws, stream=stream)
         elif wl.kv_int8:
             pa.pa_decode_attention_int8(out, d["q"], kp, vp, ks, vs, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
-                                        partition_size=args.partition, workspace=ws, stream=stream)
+                                        partition_size=partition, workspace=ws, stream=stream)
         else:
             pa.pa_decode_attention(out, d["q"], kp, vp, bt, d["ctx"], wl.scale, max_context_len=max_ctx,
-                                   partition_size=args.partition, workspace=ws, stream=stream)
+                                   partition_size=partition, workspace=ws, stream=stream)
         evs[3].record(stream)
         return evs
-    for w in range(args.warmup):
+    for w in range(warmup):
         step(w, False)
     torch.cuda.synchronize()
     # a ~50 ms device-side delay lets the host enqueue every timed step before the GPU starts on
     # them, so that the events time the GPU work and not the host's enqueue of small calls
     torch.cuda._sleep(100_000_000)
-    evl = [step(args.warmup + k, True) for k in range(args.steps)]
+    evl = [step(warmup + k, True) for k in range(reps)]
     torch.cuda.synchronize()
-    for k, e in enumerate(evl):
+    for e in evl:
         rec["append"].append(e[0].elapsed_time(e[1]) * 1e3)
         rec["prefill"].append(e[1].elapsed_time(e[2]) * 1e3)
         rec["decode"].append(e[2].elapsed_time(e[3]) * 1e3)
     med = {k: statistics.median(v) for k, v in rec.items()}
-    t_mid = (args.warmup + args.steps // 2) % wl.steps
+    p90 = {k: sorted(v)[int(0.9 * (reps - 1))] for k, v in rec.items()}
+    t_mid = (warmup + reps // 2) % wl.steps
     dec_b = wl.verify_bytes(t_mid, vq) if vq else wl.decode_bytes(t_mid)
     peak, kind = peak_hbm()
-    line = {"workload": wl.name, "description": wl.description, "steps": args.steps, "warmup": args.warmup,
-            "l2": "evicted before every step (a 512 MB read)",
-            "partition_tokens": pa.pa_decode_partition_size(S, max_ctx, kp, args.partition),
-            "append_us": med["append"], "append_gbs": wl.append_bytes() / (med["append"] * 1e-6) / 1e9,
-            "decode_us": med["decode"], "decode_p90_us": sorted(rec["decode"])[int(0.9 * (args.steps - 1))],
-            "decode_gbs": dec_b / (med["decode"] * 1e-6) / 1e9,
-            "decode_frac_of_hbm_peak": dec_b / (med["decode"] * 1e-6) / 1e9 / peak, "hbm_peak": peak,
-            "hbm_peak_kind": kind, "decode_bytes": dec_b,
-            "decode_tokens_per_s": S / ((med["append"] + med["decode"] + med["prefill"]) * 1e-6)}
+    nl = N_LAYERS.get(wl.name, 1)
+    tok_s = S / ((med["append"] + med["decode"] + med["prefill"]) * 1e-6)
+    line = {"workload": wl.name, "description": wl.description, "reps": reps, "warmup": warmup,
+            "l2": "evicted before every repetition (a read of 2x the L2 size)",
+            "partition_tokens": pa.pa_decode_partition_size(S, max_ctx, kp, partition),
+            "append_us": med["append"], "append_p90_us": p90["append"],
+            "append_gbs": wl.append_bytes() / (med["append"] * 1e-6) / 1e9,
+            "attention_us": med["decode"], "attention_p90_us": p90["decode"],
+            "attention_gbs": dec_b / (med["decode"] * 1e-6) / 1e9,
+            "attention_frac_of_hbm_peak": dec_b / (med["decode"] * 1e-6) / 1e9 / peak,
+            "hbm_peak_gbs": peak, "hbm_peak_kind": kind, "attention_bytes": dec_b,
+            "decode_tokens_per_s": tok_s, "n_layers": nl,
+            "decode_tokens_per_s_attention_only_per_model": tok_s / nl}
     if theta:
         line["rope_theta"] = theta
         line["append_note"] = "append_us covers the RoPE append of K and the in-place rotation of q"
     if wl.prompt_lens:
         fl = wl.prefill_flops()
-        line.update(prefill_us=med["prefill"], prefill_tflops=fl / (med["prefill"] * 1e-6) / 1e12,
-                    prefill_flops=fl)
+        pk, pkind = peak_bf16()
+        line.update(prefill_us=med["prefill"], prefill_p90_us=p90["prefill"],
+                    prefill_tflops=fl / (med["prefill"] * 1e-6) / 1e12,
+                    prefill_frac_of_bf16_peak=fl / (med["prefill"] * 1e-6) / 1e12 / pk,
+                    bf16_peak_tflops=pk, bf16_peak_kind=pkind, prefill_flops=fl)
     line["device_status"] = pa.pa_device_status()
+    return line
+
+
+def measure_model_step(name, pa, W, torch, dev, reps, warmup):
+    """One decode step of the whole model's attention: n_layers fused append +
+    decode calls (pa_decode_step), back to back on one stream, each layer over
+    its own K/V pool (n_layers distinct pools, together larger than L2, so every
+    layer reads its cache from HBM).  Timed with one CUDA event pair around the
+    n_layers calls, median over `reps` steps."""
+    wl = W.WORKLOADS[name]()
+    nl = N_LAYERS.get(wl.name, 1)
+    st = wl.step(0)
+    kp0, vp0 = wl.k_pool.to(dev), wl.v_pool.to(dev)
+    pools = [(kp0.clone(), vp0.clone()) for _ in range(nl)]
+    del kp0, vp0
+    bt = wl.decode_block_tables.contiguous().to(dev)
+    q, kn, vn, ctx = st.q.to(dev), st.k_new.to(dev), st.v_new.to(dev), st.context_lens.to(dev)
+    S, hq = wl.num_decode_seqs, wl.num_q_heads
+    mc = wl.max_context_len(0)
+    ws = torch.zeros(max(1, pa.pa_decode_workspace_size(S, hq, mc, pools[0][0])), dtype=torch.uint8, device=dev)
+    outs = [torch.empty_like(q) for _ in range(nl)]
+    stream = torch.cuda.current_stream()
+
+    def model_step():
+        for layer, (kp, vp) in enumerate(pools):
+            pa.pa_decode_step(outs[layer], q, kp, vp, kn, vn, bt, ctx, wl.scale, max_context_len=mc,
+                              workspace=ws, stream=stream)
+    for _ in range(warmup):
+        model_step()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(100_000_000)
+    evs = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        model_step()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    t = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    med = statistics.median(t)
+    peak, _ = peak_hbm()
+    b = nl * (wl.decode_bytes(0) + wl.append_bytes())
+    return {"n_layers": nl, "layer_pools_mb": round(nl * 2 * wl.k_pool.numel() * wl.k_pool.element_size() / 1e6, 1),
+            "model_step_us": med, "model_step_p90_us": t[int(0.9 * (reps - 1))], "per_layer_us": med / nl,
+            "gbs": b / (med * 1e-6) / 1e9, "frac_of_hbm_peak": b / (med * 1e-6) / 1e9 / peak,
+            "decode_tokens_per_s_attention_only_per_model": S / (med * 1e-6),
+            "how": f"{nl} pa_decode_step calls back to back, one per layer pool, one event pair around them"}
+
+
+def measure_configs(pa, W, torch, dev, reps=60, warmup=5):
+    flush = l2_flusher(torch, dev)
+    res = {}
+    for name in CONFIGS:
+        res[name] = measure_workload(name, pa, W, torch, dev, reps, warmup, flush=flush)
+        if name in ("llama32_1b_decode", "llama3_8b_long_b1", "llama3_8b_long_b4"):
+            res[name]["model_step"] = measure_model_step(name, pa, W, torch, dev, max(reps // 3, 20), 3)
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_other(args):
+    """Per-call figures of one workload (L2 evicted before every step)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_decode_27_gb300 import binding as pa
+    from paged_kv_decode_27_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    line = measure_workload(args.workload, pa, W, torch, dev, args.steps, args.warmup, args.partition)
     print(json.dumps(line), flush=True)
 
 

@@ -468,6 +468,19 @@ PA_API int pa_bm_get_stats(const pa_block_manager* bm, pa_bm_stats* out);
 PA_API int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs,
                           const pa_pool_desc* pool, void* stream);
 
+/*
+ * pa_copy_blocks_int8 -- pa_copy_blocks for an INT8 cache (pool->dtype =
+ * PA_I8): copies the code blocks of K and V and, with them, the blocks' rows
+ * of the K and V scale arrays (H_kv x 16 floats per block), so that the
+ * destination block dequantises to exactly the source's values (the prefix
+ * cache of "LLM Inference Server", Stage 1, over the INT8 cache of its
+ * Optional Bonus Extensions).  Bit-exact.  Pointers 16-byte aligned, pairs
+ * 8-byte aligned; ids outside the pool are skipped and set
+ * PA_DEV_BAD_BLOCK_ID.  Errors: PA_ERR_INVALID when pool->dtype is not PA_I8.
+ */
+PA_API int pa_copy_blocks_int8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                               const int32_t* pairs, int num_pairs, const pa_pool_desc* pool, void* stream);
+
 /* Bytes of the per-device array behind pa_decode_attention_noalloc. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -110,6 +110,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_bm_get_stats.argtypes = [vp, ctypes.POINTER(pa_bm_stats)]
     L.pa_copy_blocks.restype = i32
     L.pa_copy_blocks.argtypes = [vp, vp, vp, i32, pdesc, vp]
+    L.pa_copy_blocks_int8.restype = i32
+    L.pa_copy_blocks_int8.argtypes = [vp, vp, vp, vp, vp, i32, pdesc, vp]
     L.pa_append_kv_int8.restype = i32
     L.pa_append_kv_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, pdesc, vp]
     L.pa_decode_attention_int8.restype = i32
@@ -629,3 +631,19 @@ def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, pairs: torch.Tens
     _need(pairs.dtype == torch.int32 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs must be int32 [n][2]")
     _check(load_library().pa_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(pairs), int(pairs.shape[0]),
                                          ctypes.byref(desc), _stream(stream)))
+
+
+
+def pa_copy_blocks_int8(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch.Tensor,
+                        v_scales: torch.Tensor, pairs: torch.Tensor, stream=None) -> None:
+    """Copy-on-write over an INT8 cache: code blocks and their scale rows;
+    pairs: int32 CUDA [n][2] (src, dst)."""
+    desc = _pools(k_codes, v_codes)
+    for n, t in (("k_scales", k_scales), ("v_scales", v_scales), ("pairs", pairs)):
+        _cuda_contig(n, t)
+    _need(k_scales.dtype == v_scales.dtype == torch.float32 and k_scales.shape == v_scales.shape ==
+          k_codes.shape[:3], "scales must be float32 [num_blocks][H_kv][16]")
+    _need(pairs.dtype == torch.int32 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs must be int32 [n][2]")
+    _check(load_library().pa_copy_blocks_int8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+                                              _ptr(pairs), int(pairs.shape[0]), ctypes.byref(desc),
+                                              _stream(stream)))

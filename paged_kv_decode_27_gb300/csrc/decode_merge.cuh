@@ -28,32 +28,49 @@ __device__ __forceinline__ size_t query_row(const DecodeArgs& a, int s, int kvh,
   return (static_cast<size_t>(s) * a.q_len + i) * a.num_q_heads + kvh * G + h;
 }
 
+// Four consecutive outputs of one row, rounded once to T and stored together
+// (8 bytes for bf16/fp16, 16 for fp32; rows start 16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void store_out4(T* dst, float4 v) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(dst) = v;
+  } else {
+    T t[4] = {Elem<T>::from_f(v.x), Elem<T>::from_f(v.y), Elem<T>::from_f(v.z), Elem<T>::from_f(v.w)};
+    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(t);
+  }
+}
+
 // Log-sum-exp merge of the n_parts split-K partials of (sequence s, KV head
 // kvh) into the output rows: with M = max_p lse_p and w_p = 2^(lse_p - M),
 // out = sum_p w_p o_p / sum_p w_p -- the softmax over the whole context.
-// Threads tid = 0 .. nthreads-1 share the G * q_len * D outputs.
+// Threads tid = 0 .. nthreads-1 share the G * q_len * D / 4 groups of four
+// consecutive outputs; each thread keeps the loads of kBatch partials (their
+// lse and a float4 of their output) in flight together, so a merge of up to
+// kBatch partitions costs about one L2 round trip per group it owns.
 template <typename T, int D>
 __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int s, int kvh, int G, int n_parts,
                                                      int tid, int nthreads) {
   T* out = static_cast<T*>(a.out);
   const int ncols = G * a.q_len;
-  constexpr int kBatch = 8;   // partials whose loads are in flight together
-  for (int idx = tid; idx < ncols * D; idx += nthreads) {
-    const int c = idx / D;
-    const int d = idx - c * D;
+  constexpr int V4 = D / 4;       // float4 groups per row
+  constexpr int kBatch = 16;      // partials whose loads are in flight together
+  for (int idx = tid; idx < ncols * V4; idx += nthreads) {
+    const int c = idx / V4;
+    const int d4 = idx - c * V4;
     const size_t qr = query_row(a, s, kvh, G, c);
     const size_t row0 = qr * a.max_splits;
-    // a running max over batches of partitions; each batch issues all of its
-    // loads before any arithmetic, so the merge costs ~one memory latency per
-    // batch instead of one per partition
-    float M = -INFINITY, L = 0.f, O = 0.f;
+    // a running max over batches of partitions
+    float M = -INFINITY, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int p0 = 0; p0 < n_parts; p0 += kBatch) {
-      float lp[kBatch], op[kBatch];
+      float lp[kBatch];
+      float4 op[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const bool in = p0 + k < n_parts;
         lp[k] = in ? __ldcg(a.ws_lse + row0 + p0 + k) : -INFINITY;
-        op[k] = in ? __ldcg(a.ws_o + (row0 + p0 + k) * D + d) : 0.f;
+        op[k] = in ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + (row0 + p0 + k) * D) + d4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float mb = M;
 #pragma unroll
@@ -61,16 +78,23 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int s,
       if (mb == -INFINITY) continue;
       const float r = exp2f(M - mb);      // 0 while M is still -inf
       L *= r;
-      O *= r;
+      O.x *= r;
+      O.y *= r;
+      O.z *= r;
+      O.w *= r;
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const float w = exp2f(lp[k] - mb);   // 0 for empty partitions
         L += w;
-        O = fmaf(w, op[k], O);
+        O.x = fmaf(w, op[k].x, O.x);
+        O.y = fmaf(w, op[k].y, O.y);
+        O.z = fmaf(w, op[k].z, O.z);
+        O.w = fmaf(w, op[k].w, O.w);
       }
       M = mb;
     }
-    out[qr * D + d] = Elem<T>::from_f(L > 0.f ? O / L : 0.f);
+    const float4 o = L > 0.f ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L) : make_float4(0.f, 0.f, 0.f, 0.f);
+    store_out4<T>(out + qr * D + 4 * d4, o);
   }
 }
 

@@ -66,6 +66,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const int G = a.num_q_heads / a.num_kv_heads;
 
   grid_dependency_wait();   // inputs may come from the kernel just before us
+  // The next kernel launched with programmatic serialisation (a decode of the
+  // next layer, say) may be scheduled once every CTA of this grid is running;
+  // it waits for this grid's completion before it reads or writes anything.
+  allow_dependents();
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  // This warp's block-table entries of the partition (warp w takes blocks w,
+  // w + W, ...), one per lane, loaded before the context length is known so
+  // that the two loads overlap: entries below max_blocks_per_seq always exist.
+  const int blk0 = split * a.part_blocks;
+  const int jl = warp + lane * W;   // partition-local block of this lane
+  int my_id = 0;
+  if (jl < a.part_blocks && blk0 + jl < a.max_blocks_per_seq)
+    my_id = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + blk0 + jl);
+  // Decode step with the append fused in: this sequence's new K and V rows of
+  // this KV head, 16 bytes per lane (K in lanes 0..CH-1, V in CH..2CH-1).
+  constexpr int CH = D * static_cast<int>(sizeof(T)) / 16;
+  uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+  if (a.k_new != nullptr && lane < 2 * CH) {
+    const bool is_v = lane >= CH;
+    new_row = __ldg(static_cast<const uint4*>(is_v ? a.v_new : a.k_new) +
+                    (static_cast<size_t>(s) * a.num_kv_heads + kvh) * CH + (is_v ? lane - CH : lane));
+  }
   const int ctx = checked_context(a, s, threadIdx.x == 0 && split == 0 && kvh == 0);
   const int nblk_seq = (ctx + kBlock - 1) / kBlock;
   const int n_splits = (nblk_seq + a.part_blocks - 1) / a.part_blocks;
@@ -74,32 +99,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     return;
   }
   if (split >= n_splits) return;
-  if (a.k_new != nullptr && split == n_splits - 1) {
-    // decode step with the append fused in: write this step's token, then let
-    // the TMA copies below (async proxy) see it
-    write_step_token<T, D>(a, s, kvh, ctx, W * 32);
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    __syncthreads();
-  }
-  const int blk0 = split * a.part_blocks;
   const int nblk = min(a.part_blocks, nblk_seq - blk0);
   const int nb_w = nblk > warp ? (nblk - warp + W - 1) / W : 0;   // <= 32 (host limit)
 
-  // Physical ids of this warp's blocks, one per lane; out-of-range ids are
-  // replaced by block 0 and their tokens masked out.
-  int my_id = 0;
+  // Out-of-range ids are replaced by block 0 and their tokens masked out.
   bool my_bad = false;
   if (lane < nb_w) {
-    int id = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + blk0 + warp +
-                   lane * W);
-    if (id < 0 || id >= a.num_blocks) {
+    if (my_id < 0 || my_id >= a.num_blocks) {
       my_bad = true;
-      id = 0;
+      my_id = 0;
       flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
     }
-    my_id = id;
+  } else {
+    my_id = 0;
   }
   const unsigned bad_mask = __ballot_sync(0xffffffffu, my_bad);
+
+  if (a.k_new != nullptr && split == n_splits - 1 && warp == (nblk - 1) % W) {
+    // The new token (position ctx - 1) lies in the sequence's last block, which
+    // this warp reads: write it, then order the writes before the warp's own
+    // TMA copies (async proxy) of that block.
+    const int li = (nblk - 1) / W;   // lane holding the block's id
+    const int id = __shfl_sync(0xffffffffu, my_id, li);
+    if (!((bad_mask >> li) & 1u) && lane < 2 * CH) {
+      const size_t row = (static_cast<size_t>(id) * a.num_kv_heads + kvh) * kBlock + (ctx - 1) % kBlock;
+      const bool is_v = lane >= CH;
+      uint4* pool = static_cast<uint4*>(const_cast<void*>(is_v ? a.v_pool : a.k_pool));
+      pool[row * CH + (is_v ? lane - CH : lane)] = new_row;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+  }
 
   const uint32_t wbase = smem_u32(smem + warp * NS * STAGE);
   const uint32_t bar0 = smem_u32(&bars[warp * NS]);
@@ -107,8 +137,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   if (lane == 0) {
     for (int st = 0; st < NS; ++st) mbar_init(bar0 + 8 * st, 1);
     fence_barrier_init();
-    prefetch_tensormap(&kmap);
-    prefetch_tensormap(&vmap);
   }
   __syncwarp();
 
@@ -315,11 +343,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
 namespace {
 
-template <typename T, int D>
-cudaError_t launch_tc_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        cudaStream_t stream) {
+template <typename T, int D, int NS>
+cudaError_t launch_tc_ns(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         cudaStream_t stream) {
   constexpr int W = 4;
-  constexpr int NS = (D == 128) ? 2 : 4;   // 3 CTAs per SM either way (64 KB of stages)
   constexpr int STAGE = 2 * (D / 64) * 16 * 128;
   static_assert(W * 8 * D * 4 + W * 16 * 4 <= W * NS * STAGE, "merge buffer must fit");
   const int smem = W * NS * STAGE + 1024;
@@ -328,6 +355,22 @@ cudaError_t launch_tc_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUte
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
   return launch_pdl(kern, grid, dim3(W * 32), smem, stream, kmap, vmap, a);
+}
+
+// Stages per warp: 64 KB of stages per CTA fits three CTAs on an SM (192 KB in
+// flight per SM).  When the grid has fewer CTAs than that per SM, each CTA
+// takes the stages the absent ones would have used (96 or 192 KB), so that
+// small batches keep as many bytes in flight per SM as large ones.
+template <typename T, int D>
+cudaError_t launch_tc_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        cudaStream_t stream) {
+  constexpr int NS1 = (D == 128) ? 2 : 4;   // 16 KB per warp
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 152;
+  const long long ctas = static_cast<long long>(a.max_splits) * a.num_kv_heads * a.num_seqs;
+  if (ctas <= sms) return launch_tc_ns<T, D, 3 * NS1>(a, kmap, vmap, stream);
+  if (ctas <= 2LL * sms) return launch_tc_ns<T, D, 3 * NS1 / 2>(a, kmap, vmap, stream);
+  return launch_tc_ns<T, D, NS1>(a, kmap, vmap, stream);
 }
 
 }  // namespace

@@ -795,9 +795,34 @@ int pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pai
   int* status = status_ptr();
   if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
   const int block_bytes = pool->num_kv_heads * PA_BLOCK_SIZE * pool->head_dim * elem_bytes(pool->dtype);
-  cudaError_t e = pa::launch_copy_blocks(k_pool, v_pool, pairs, num_pairs, block_bytes, pool->num_blocks, status,
+  pa::CopyArrays arrs{{k_pool, v_pool, nullptr, nullptr}, {block_bytes / 16, block_bytes / 16, 0, 0}};
+  cudaError_t e = pa::launch_copy_blocks(arrs, 2, pairs, num_pairs, pool->num_blocks, status,
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PA_OK;
+}
+
+int pa_copy_blocks_int8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const int32_t* pairs,
+                        int num_pairs, const pa_pool_desc* pool, void* stream) {
+  t_err.clear();
+  int rc = check_pool(pool);
+  if (rc != PA_OK) return rc;
+  if (pool->dtype != PA_I8) return fail(PA_ERR_INVALID, "pool dtype must be PA_I8 for an INT8 cache");
+  if (num_pairs < 0) return fail(PA_ERR_INVALID, "num_pairs must be >= 0");
+  if (num_pairs == 0) return PA_OK;
+  if (!k_codes || !v_codes || !k_scales || !v_scales || !pairs) return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales) ||
+      (reinterpret_cast<uintptr_t>(pairs) & 7u))
+    return fail(PA_ERR_INVALID, "codes and scales must be 16-byte and pairs 8-byte aligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  const int code_bytes = pool->num_kv_heads * PA_BLOCK_SIZE * pool->head_dim;   // one byte per code
+  const int scale_bytes = pool->num_kv_heads * PA_BLOCK_SIZE * static_cast<int>(sizeof(float));
+  pa::CopyArrays arrs{{k_codes, v_codes, k_scales, v_scales},
+                      {code_bytes / 16, code_bytes / 16, scale_bytes / 16, scale_bytes / 16}};
+  cudaError_t e = pa::launch_copy_blocks(arrs, 4, pairs, num_pairs, pool->num_blocks, status,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks_int8 launch");
   return PA_OK;
 }
 

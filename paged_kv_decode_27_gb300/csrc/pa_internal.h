@@ -114,8 +114,14 @@ cudaError_t launch_apply_rope(void* x, const int32_t* positions, const float* co
                               int num_tokens, int num_heads, int head_dim, int dtype, int* status,
                               cudaStream_t stream);
 
-// Copy-on-write: whole pool blocks (all heads, K and V), pairs (src, dst) on the device.
-cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* pairs, int num_pairs, int block_bytes,
+// Copy-on-write: whole blocks of up to four block-indexed arrays (K and V
+// pools; for an INT8 cache also the K and V scale arrays), pairs (src, dst)
+// on the device.  chunks_per_block = 16-byte chunks of one block in that array.
+struct CopyArrays {
+  void* ptr[4];
+  int chunks_per_block[4];
+};
+cudaError_t launch_copy_blocks(const CopyArrays& arrs, int num_arrays, const int32_t* pairs, int num_pairs,
                                int num_blocks, int* status, cudaStream_t stream);
 
 // Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).

@@ -274,3 +274,16 @@ def test_decode_step_validates_on_the_host(lib):
     assert call(kn=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
     assert call(kn=ctypes.c_void_p(FAKE + 8)) == B.PA_ERR_INVALID
     assert call(d=_desc(dt=B.PA_I8)) == B.PA_ERR_INVALID
+
+
+def test_copy_blocks_validate_on_the_host(lib):
+    f = ctypes.c_void_p(FAKE)
+    cp = lambda desc, n=2, pairs=f: lib.pa_copy_blocks(f, f, pairs, n, ctypes.byref(desc), None)
+    cp8 = lambda desc, n=2, pairs=f, ks=f: lib.pa_copy_blocks_int8(f, f, ks, f, pairs, n, ctypes.byref(desc), None)
+    assert cp(_desc(dt=B.PA_I8)) == B.PA_ERR_INVALID            # an INT8 cache has its own call
+    assert cp8(_desc(dt=B.PA_BF16)) == B.PA_ERR_INVALID         # and it takes INT8 pools only
+    assert cp8(_desc(dt=B.PA_I8), n=-1) == B.PA_ERR_INVALID
+    assert cp8(_desc(dt=B.PA_I8), n=0) == B.PA_OK                # nothing to copy
+    assert cp8(_desc(dt=B.PA_I8), ks=ctypes.c_void_p(FAKE + 4)) == B.PA_ERR_INVALID   # scales not 16-byte aligned
+    assert cp8(_desc(dt=B.PA_I8), pairs=ctypes.c_void_p(FAKE + 4)) == B.PA_ERR_INVALID
+    assert cp8(_desc(dt=B.PA_I8), ks=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
