@@ -211,6 +211,27 @@ int make_pool_map(CUtensorMap* map, const void* pool_ptr, const pa_pool_desc* po
   return PA_OK;
 }
 
+// The prompt-pass queries q [rows][H][D] viewed as a 3-D tensor (D, H, rows)
+// for 128-row boxes of one head and 64 columns (128 bytes, 128-byte swizzle):
+// one box is half of a query tile in the layout the S product reads.  `rows`
+// is an upper bound of the query rows; the kernel loads by this map only
+// whole 128-row tiles of a prompt, which lie inside the caller's buffer.
+int make_q_map(CUtensorMap* map, const void* q, int dtype, int num_heads, int head_dim, long long rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapDataType dt = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                           static_cast<cuuint64_t>(num_heads) * head_dim * 2};
+  cuuint32_t box[3] = {64u, 1u, 128u};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled (queries) failed (%d)", static_cast<int>(r));
+  return PA_OK;
+}
+
 // Small per-thread cache: encoding is cheap but not free, and the same pools
 // are passed on every step.
 struct MapEntry {
@@ -592,10 +613,13 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   a.num_blocks = pool->num_blocks;
   a.max_q_len = max_q_len;
   a.status = status;
-  CUtensorMap kmap, vmap;
+  CUtensorMap kmap, vmap, qmap;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
-  cudaError_t e = pa::launch_prefill_umma(a, pool->dtype, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if ((rc = make_q_map(&qmap, q, pool->dtype, num_q_heads, pool->head_dim,
+                       static_cast<long long>(num_seqs) * max_q_len)) != PA_OK)
+    return rc;
+  cudaError_t e = pa::launch_prefill_umma(a, pool->dtype, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PA_OK;
 }

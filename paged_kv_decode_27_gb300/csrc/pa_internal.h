@@ -125,8 +125,9 @@ cudaError_t launch_copy_blocks(const CopyArrays& arrs, int num_arrays, const int
                                int num_blocks, int* status, cudaStream_t stream);
 
 // Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).
+// qmap: the queries as (D, H, rows) in 128-row x 64-column boxes (whole query tiles only).
 cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, cudaStream_t stream);
+                                const CUtensorMap& vmap, const CUtensorMap& qmap, cudaStream_t stream);
 
 
 }  // namespace pa

@@ -6,43 +6,57 @@
 // From Scratch", What you build: fused attention with causal masking; How it
 // works, 4 Attention Kernel: causal mask, GQA).  It is a dense contraction and
 // compute-bound ("LLM Inference Server", What You Will Build), so it runs on
-// tcgen05.mma:
+// tcgen05.mma.
 //
-//  * One CTA per SM works on two consecutive 128-row query tiles of one head
-//    (A = rows 256t..256t+127, B = the next 128), which share every K/V tile
-//    they both need; a 1-D grid puts the latest (longest) tile pairs first.
-//    Ten warps with fixed roles:
-//      warps 0-3 / 4-7  softmax for tile A / B: thread r owns query row r.  It
-//                 reads its row of S = Q K^T from tensor memory, applies the
-//                 causal mask and the online softmax, writes its row of P
-//                 (bf16/fp16) back over S and, when its running max grows,
-//                 rescales its row of O;
-//      warp 8     TMA producer: K tiles and V tiles of 128 keys (8 pool
-//                 blocks, read through the block table, whose entries the warp
-//                 loads up front) into two 2-stage rings of 128-byte-swizzled
-//                 shared memory;
-//      warps 9/10 MMA issuers for tile A / B: S = Q K^T (M=128, N=128, K=D; Q
-//                 and K from shared memory) and O += P V (M=128, N=D, K=128; P
-//                 from tensor memory, V read MN-major straight from its pool
-//                 layout).  One issuer per tile, because issuing stalls while
-//                 the tensor pipe is busy and must not hold up the other tile.
-//    Producer and issuers block in mbarrier.try_wait on the next input they
-//    need, leaving the issue slots to the softmax warps.
-//    N = 128 keys per S tile: with the A operand in shared memory a narrower
-//    MMA costs as much as this one.
-//  * Tensor memory (all 512 columns): per tile one S/P buffer of 128 columns
-//    and O (D columns).  The two tiles ping-pong: while one tile's softmax
-//    runs, the tensor cores work on the other tile's S and PV.
-//  * A K stage is released once every S MMA that reads it completes, a V
-//    stage once every PV MMA that reads it completes.
-//  * O is rescaled lazily: only when a row's max grows by more than 2^8 (so
-//    probabilities stay <= 256, exact in the final normalisation).
-//  * Query i of a sequence with context c and q_len n sits at position
-//    c - n + i and sees keys 0..c - n + i; value rows past the context are
-//    zeroed in shared memory so stale pool data never reaches the output.
+// Work.  One item = one 128-row query tile of one sequence for two q heads of
+// the same KV head (tile A = head 2p, tile B = head 2p + 1; one head per item
+// when the query group is odd).  The two tiles need the same K/V tiles in the
+// same order and as many of them, so every K/V tile is read into shared
+// memory once for both: the bytes an SM receives per product are what bound
+// this kernel once its MMAs are pipelined.  The grid is persistent (one CTA
+// per SM): each CTA sorts the (sequence, query tile) pairs by their number of
+// key tiles, longest first, in shared memory, and the items (a pair and a
+// head pair) are dealt to the CTAs round by round in snake order.
 //
-// Every wait is bounded; a timeout sets PA_DEV_WAIT_TIMEOUT, lets the copies
-// and MMAs in flight finish (bounded) and frees the tensor memory.
+// Per K tile j of an item (128 keys = 8 pool blocks) and per tile g:
+//   S_g = Q_g K^T  (M = 128 query rows, N = 128 keys, K = D; Q and K from
+//                   128-byte swizzled shared memory) into tensor memory;
+//   softmax        one thread per query row reads its row of S, applies the
+//                   causal mask and the online softmax (log2 domain, the
+//                   running reference raised lazily: only when a row's
+//                   maximum grows by more than 2^8), writes P (bf16/fp16
+//                   pairs) over S;
+//   O_g += P_g V   (M = 128, N = D, K = 128 keys; P from tensor memory, V read
+//                   MN-major straight from its pool layout).
+// One thread issues both tiles' products, interleaved so that one tile's
+// products run during the other's softmax.  It issues S for K tile j + 1
+// right after PV for tile j: the MMAs of one thread run in issue order, so
+// S_{j+1} overwrites the columns of P_j only after PV_j has read them, and
+// the next S needs no wait on the PV's completion.
+//
+// Tensor memory (512 columns): per tile S/P (128 columns) and O (D columns).
+// Shared memory: Q_A, Q_B, a 2-stage K ring and a 2-stage V ring, the sorted
+// work list.
+//
+// Warps (384 threads, three warpgroups that re-balance their registers with
+// setmaxnreg):
+//   0-3 / 4-7  softmax of tile A / B (thread r owns query row r), and at the
+//              end of an item the epilogue: normalise O and store the rows;
+//   8 / 10     TMA producers of the K ring / the V ring (pool rows through the
+//              block table);
+//   9          MMA issuer of both tiles (one elected lane), in the interleaved
+//              order below;
+//   11         query loader: the next item's Q tiles (TMA; cp.async for a
+//              prompt's last partial tile), once the current item's S
+//              products have completed.
+// Every hand-off is an mbarrier; every wait is bounded, and a timeout sets
+// PA_DEV_WAIT_TIMEOUT, lets the copies and MMAs in flight finish (bounded)
+// and frees the tensor memory.
+//
+// Query i of a sequence with context c and q_len n sits at position
+// c - n + i and sees keys 0..c - n + i; value rows past the context are zeroed
+// in shared memory (and whole blocks past it read as zero), so stale pool data
+// never reaches the output.
 #include <type_traits>
 
 #include "pa_common.cuh"
@@ -52,461 +66,645 @@ namespace pa {
 
 namespace {
 
-constexpr int kRows = 128;     // query rows per tile (MMA M)
-constexpr int kKeys = 128;     // keys per K/V tile (8 pool blocks)
-constexpr int kStages = 2;     // K and V ring depth
+constexpr int kRows = 128;      // query rows per tile (MMA M)
+constexpr int kKeys = 128;      // keys per K/V tile (MMA N of S, K of PV)
+constexpr int kStagesK = 2;     // K ring depth
+constexpr int kStagesV = 3;     // V ring depth: a V stage waits longest to be refilled (the PV of both tiles)
 constexpr int kBlocksPerTile = kKeys / 16;
-constexpr int kThreads = 352;  // 2 x 4 softmax warps + producer warp + one MMA warp per tile
+constexpr int kThreads = 384;   // three warpgroups
 constexpr int kTmemCols = 512;
+constexpr int kMaxPairs = 384;    // (sequence, query tile) pairs sorted in shared memory
+constexpr int kMaxCost = 63;      // key tiles per query tile, for the sort's buckets (longer share the last)
+// Registers per thread after the warpgroups re-balance the launch's
+// 168 x 384 = 64512: (200 + 200 + 96) x 128 = 63488 <= 64512, so the
+// increases never wait for registers that are not there.
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsIo = 96;
+static_assert((2 * kRegsSoftmax + kRegsIo) * 128 <= 168 * kThreads, "register split");
 
 template <int D>
 struct UmmaLayout {
   static constexpr int NBOX = D / 64;                 // 128-byte column boxes per row
   static constexpr int Q_BYTES = kRows * D * 2;       // one Q tile: [NBOX][128 rows][128 B]
   static constexpr int KT_BYTES = kKeys * D * 2;      // one K (or V) tile: [NBOX][128 rows][128 B]
-  static constexpr int K_OFF = 2 * Q_BYTES;
-  static constexpr int V_OFF = K_OFF + kStages * KT_BYTES;
-  static constexpr int SMEM = V_OFF + kStages * KT_BYTES;
   static constexpr int HALF_Q = kRows * 128;          // one 64-column box strip of Q
   static constexpr int HALF_KT = kKeys * 128;         // one 64-column box strip of K or V
+  static constexpr int K_OFF = 2 * Q_BYTES;
+  static constexpr int V_OFF = K_OFF + kStagesK * KT_BYTES;
+  static constexpr int PAIRS_OFF = V_OFF + kStagesV * KT_BYTES;  // int32 [kMaxPairs]
+  static constexpr int HIST_OFF = PAIRS_OFF + kMaxPairs * 4;     // int32 [kMaxCost + 1]
+  static constexpr int SMEM = HIST_OFF + (kMaxCost + 1) * 4;
   static constexpr uint32_t TMEM_TILE = 256;          // columns per query tile
   static constexpr uint32_t TMEM_S = 0;               // S: kKeys fp32 columns (P packed over its first half)
   static constexpr uint32_t TMEM_O = kKeys;           // O: D fp32 columns
 };
+
+// One work item: query tile t (rows 128t ..) of sequence s, q heads h (tile A)
+// and h + 1 (tile B, when paired).
+struct Item {
+  int s, h, t, q0, n, c, nkt;
+};
+
+__device__ __forceinline__ int key_tiles(int c, int n, int t) {
+  // the tile's last row sits at position c - n + min(128 (t + 1), n) - 1
+  return (c - n + min(kRows * (t + 1), n) - 1) / kKeys + 1;
+}
 
 }  // namespace
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                    const PrefillArgs a) {
+                    const __grid_constant__ CUtensorMap qmap, const PrefillArgs a) {
   using L = UmmaLayout<D>;
   constexpr int NBOX = L::NBOX;
   constexpr bool kBf16 = !std::is_same<T, __half>::value;
 
   extern __shared__ uint8_t smem_raw[];
-  // k_full[2] v_full[2] | k_empty[2 tiles][2] v_empty[2 tiles][2] | s_full p_full pv_done mma_final [2 tiles].
-  // Every waiter waits on a phase that cannot be overtaken before it has
-  // waited: a barrier's next phase always depends on the waiter's progress.
-  __shared__ __align__(8) uint64_t bars[20];
+  // k_full[2] k_empty[2] v_full[3] v_empty[3] | s_full[2] p_full[2] pv_done[2] o_free[2] |
+  // q_full[2] q_empty[2] | mma_final
+  __shared__ __align__(8) uint64_t bars[23];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
+  __shared__ int n_pairs_sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sK = sQ + L::K_OFF;
   const uint32_t sV = sQ + L::V_OFF;
+  int* pairs = reinterpret_cast<int*>(smem + L::PAIRS_OFF);
+  int* hist = reinterpret_cast<int*>(smem + L::HIST_OFF);
 
-  // latest tile pairs first: the pair index descends slowest over the 1-D grid
-  const int per_layer = a.num_q_heads * a.num_seqs;
-  const int pt = (gridDim.x / per_layer) - 1 - static_cast<int>(blockIdx.x) / per_layer;
-  const int hq = static_cast<int>(blockIdx.x) % a.num_q_heads;
-  const int s = (static_cast<int>(blockIdx.x) % per_layer) / a.num_q_heads;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int G = a.num_q_heads / a.num_kv_heads;
-  const int kvh = hq / G;
-
-  grid_dependency_wait();   // the prompt's K/V were appended by the kernel before us
-  const int q0 = __ldg(a.cu_q_lens + s);
-  const int n = __ldg(a.cu_q_lens + s + 1) - q0;
-  int c = __ldg(a.context_lens + s);
-  const int cap = a.max_blocks_per_seq * kBlock;
-  if (c < n || c > cap || n < 0 || n > a.max_q_len) {
-    if (threadIdx.x == 0 && pt == 0 && hq == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
-    c = c > cap ? cap : c;
-    if (c < n || n > a.max_q_len) return;
-  }
-  // tile g of the pair: query rows qr0[g] .. qr0[g]+127; n_kt[g] key tiles (0 = no rows)
-  int nkt_g[2];
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const int qr = (2 * pt + g) * kRows;
-    nkt_g[g] = qr < n ? (c - n + qr + min(kRows, n - qr) - 1) / kKeys + 1 : 0;
-  }
-  if (nkt_g[0] == 0) return;
-  const int n_kt = nkt_g[1] > nkt_g[0] ? nkt_g[1] : nkt_g[0];
+  const int H = a.num_q_heads;
+  const int G = H / a.num_kv_heads;
+  const bool paired = (G % 2) == 0;     // tile B exists
+  const int NT = paired ? 2 : 1;        // query tiles per item
+  const int HG = H / NT;                // head groups per (sequence, query tile)
 
   const uint32_t bar0 = smem_u32(&bars[0]);
   auto k_full = [&](int i) { return bar0 + 8u * i; };
-  auto v_full = [&](int i) { return bar0 + 16u + 8u * i; };
-  auto k_empty = [&](int g, int i) { return bar0 + 32u + 16u * g + 8u * i; };
-  auto v_empty = [&](int g, int i) { return bar0 + 64u + 16u * g + 8u * i; };
-  auto s_full = [&](int g) { return bar0 + 96u + 8u * g; };
-  auto p_full = [&](int g) { return bar0 + 112u + 8u * g; };
-  auto pv_done = [&](int g) { return bar0 + 128u + 8u * g; };
-  auto mma_final = [&](int g) { return bar0 + 144u + 8u * g; };
+  auto k_empty = [&](int i) { return bar0 + 16u + 8u * i; };
+  auto v_full = [&](int i) { return bar0 + 32u + 8u * i; };
+  auto v_empty = [&](int i) { return bar0 + 56u + 8u * i; };
+  auto s_full = [&](int g) { return bar0 + 80u + 8u * g; };
+  auto p_full = [&](int g) { return bar0 + 96u + 8u * g; };
+  auto pv_done = [&](int g) { return bar0 + 112u + 8u * g; };
+  auto o_free = [&](int g) { return bar0 + 128u + 8u * g; };
+  auto q_full = [&](int g) { return bar0 + 144u + 8u * g; };
+  auto q_empty = [&](int g) { return bar0 + 160u + 8u * g; };
+  auto mma_final = [&](int g) { return bar0 + 176u + 8u * g; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kStagesK; ++i) {
       mbar_init(k_full(i), 1);
+      mbar_init(k_empty(i), 1);   // released once every product reading the stage has completed
+    }
+    for (int i = 0; i < kStagesV; ++i) {
       mbar_init(v_full(i), 1);
+      mbar_init(v_empty(i), 1);
     }
     for (int g = 0; g < 2; ++g) {
-      for (int i = 0; i < kStages; ++i) {
-        mbar_init(k_empty(g, i), 1);
-        mbar_init(v_empty(g, i), 1);
-      }
       mbar_init(s_full(g), 1);
       mbar_init(p_full(g), 4);
       mbar_init(pv_done(g), 1);
-      mbar_init(mma_final(g), 1);
+      mbar_init(o_free(g), 4);
+      mbar_init(q_full(g), 1);
+      mbar_init(q_empty(g), 1);
     }
+    mbar_init(mma_final(0), 1);
     fence_barrier_init();
     abort_sh = 0;
+    n_pairs_sh = 0;
   }
-  // The barriers are ready: the producer starts streaming K/V tiles at once, while
-  // the other warps allocate tensor memory and stage Q (they meet on named barrier 1).
-  __syncthreads();
-  uint32_t tmem = 0;
-  if (warp != 8) {
-    if (warp == 0) {
-      tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
-      tmem_relinquish();
-    }
-    // Q tiles -> shared memory in the 128-byte-swizzled K-major layout; every load of a
-    // row is in flight before the first store
-    if (warp < 8) {
-      const int g = warp >> 2;
-      const int r = threadIdx.x & 127;
-      const int lr = (2 * pt + g) * kRows + r;
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
-                                                        ((static_cast<size_t>(q0) + lr) * a.num_q_heads + hq) * D);
-      const uint32_t qbase = sQ + g * L::Q_BYTES;
-      uint4 v[D / 8];
-#pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) v[cc] = lr < n ? src[cc] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) {
-        const uint32_t dst = qbase + (cc >> 3) * L::HALF_Q + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v[cc].x), "r"(v[cc].y), "r"(v[cc].z),
-                     "r"(v[cc].w)
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-    }
-    tc_fence_before_sync();
-    asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");   // every warp but the producer
-    tc_fence_after_sync();
-    tmem = tmem_base_sh;
+  if (warp == 0) {
+    __syncwarp();   // thread 0 has left the set-up above: the allocation is warp-wide
+    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tmem_relinquish();
   }
+  if (warp == 8 && lane == 0) prefetch_tensormap(&kmap);
+  if (warp == 10 && lane == 0) prefetch_tensormap(&vmap);
+  if (warp == 11 && lane == 0) prefetch_tensormap(&qmap);
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    // The whole warp runs the loop (lane 0 issues the copies).  Pool row
-    // coordinates of the blocks are read up front, 128 blocks at a time, spread
-    // over the lanes (lane l holds blocks l, l+32, l+64, l+96 of the chunk).
-    if (lane == 0) {
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
-    }
-    const uint64_t policy = l2_policy_evict_last();   // other heads of the group re-read these tiles
-    const int oob_row = a.num_blocks * a.num_kv_heads * kBlock;   // rows past the pool read as zero
-    const int nblk = n_kt * kBlocksPerTile;
-    int yr[4];
-    int chunk = -1;
-    auto load_chunk = [&](int ch) {
+  grid_dependency_wait();   // the prompt's K/V were appended by the kernel before us
+
+  // ---- the work list: (sequence, query tile) pairs sorted by key tiles, most
+  // first (a counting sort; within a bucket the order does not matter).
+  const int cap = a.max_blocks_per_seq * kBlock;
+  auto seq_load = [&](int s, int& q0, int& n, int& c) {
+    q0 = __ldg(a.cu_q_lens + s);
+    n = __ldg(a.cu_q_lens + s + 1) - q0;
+    c = __ldg(a.context_lens + s);
+  };
+  auto seq_shape = [&](int s, int& q0, int& n, int& c) -> bool {
+    seq_load(s, q0, n, c);
+    return n > 0 && n <= a.max_q_len && c >= n && c <= cap;
+  };
+  for (int i = threadIdx.x; i <= kMaxCost; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < a.num_seqs; s += kThreads) {
+    int q0, n, c;
+    const bool ok = seq_shape(s, q0, n, c);
+    if (!ok && !(n == 0 && c >= 0 && c <= cap) && blockIdx.x == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+    if (!ok) continue;
+    const int nt = (n + kRows - 1) / kRows;
+    atomicAdd(&n_pairs_sh, nt);
+    for (int t = 0; t < nt; ++t) atomicAdd(&hist[min(key_tiles(c, n, t), kMaxCost)], 1);
+  }
+  __syncthreads();
+  const int n_pairs = n_pairs_sh;
+  const bool sorted = n_pairs <= kMaxPairs;
+  if (sorted) {
+    if (warp == 0) {
+      // exclusive prefix over the buckets, most key tiles first: lane l sums a
+      // contiguous run of 32 buckets (from the top), then a warp scan
+      const int per = (kMaxCost + 1) / 32;
+      const int hi = kMaxCost - lane * per;   // this lane's buckets: hi, hi-1, ..., hi-per+1
+      int run = 0;
+      for (int i = 0; i < per; ++i) run += hist[hi - i];
+      int incl = run;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int lb = ch * 128 + k * 32 + lane;
-        int y = oob_row;
-        if (lb < nblk && lb * kBlock < c) {
-          const int id = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + lb);
-          if (id >= 0 && id < a.num_blocks)
-            y = (id * a.num_kv_heads + kvh) * kBlock;
-          else
-            flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
-        }
-        yr[k] = y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      chunk = ch;
-    };
-    // One box (16 rows x 128 bytes) per lane: a single issuing thread would
-    // serialise the tile's kBlocksPerTile * NBOX tensor copies.
-    auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
-      const int lb0 = j * kBlocksPerTile;              // a tile's blocks never straddle a 32-block group
-      if ((lb0 >> 7) != chunk) load_chunk(lb0 >> 7);
-      const int k = (lb0 >> 5) & 3;
-      const int v = k == 0 ? yr[0] : k == 1 ? yr[1] : k == 2 ? yr[2] : yr[3];
-      const int b = lane % kBlocksPerTile;
-      const int h = lane / kBlocksPerTile;
-      const int y = __shfl_sync(0xffffffffu, v, (lb0 + b) & 31);
-      if (lane == 0) mbar_arrive_expect_tx(bar, L::KT_BYTES);
-      __syncwarp();
-      if (h < NBOX) tma_load_2d(dst + h * L::HALF_KT + b * 2048, map, h * 64, y, bar, policy);
-      __syncwarp();
-    };
-    // Fixed order K_0 V_0 K_1 V_1 ...: K_{j+2} reuses the stage freed by the S
-    // MMAs of tile j, V_{j+2} the one freed by its PV MMAs.  The warp blocks
-    // (suspended in mbarrier.try_wait) on exactly the next release it needs.
-    auto stage_free = [&](bool is_k, int j) -> bool {   // all lanes
-      if (j < kStages) return true;
-      const int jp = j - kStages;
-      bool ok2 = true;
+      int off = incl - run;
+      for (int i = 0; i < per; ++i) {
+        const int cnt = hist[hi - i];
+        hist[hi - i] = off;
+        off += cnt;
+      }
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s < a.num_seqs; s += kThreads) {
+      int q0, n, c;
+      if (!seq_shape(s, q0, n, c)) continue;
+      const int nt = (n + kRows - 1) / kRows;
+      for (int t = 0; t < nt; ++t) {
+        const int pos = atomicAdd(&hist[min(key_tiles(c, n, t), kMaxCost)], 1);
+        pairs[pos] = (s << 16) | t;
+      }
+    }
+  }
+  // Without the sorted list (too many pairs), items run over every
+  // (query tile, sequence, head group) in order of decreasing tile, skipping empty ones.
+  const int t_max = (a.max_q_len + kRows - 1) / kRows;
+  const long long n_items = sorted ? static_cast<long long>(n_pairs) * HG
+                                   : static_cast<long long>(t_max) * a.num_seqs * HG;
+  // Items are dealt round by round, in snake order (round m gives CTA b the
+  // item m * grid + b, or m * grid + grid - 1 - b when m is odd), so that the
+  // CTA with the longest item of one round gets the shortest of the next.
+  // The first item of round m or later that has work; false when none is left.
+  auto find_item = [&](long long& m, Item& it) -> bool {
+    for (;; ++m) {
+      const long long k = m * gridDim.x + ((m & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+      if (k >= n_items) return false;
+      it.h = static_cast<int>(k % HG) * NT;
+      if (sorted) {
+        const int p = pairs[k / HG];
+        it.s = p >> 16;
+        it.t = p & 0xffff;
+      } else {
+        const long long r = k / HG;
+        it.s = static_cast<int>(r % a.num_seqs);
+        it.t = t_max - 1 - static_cast<int>(r / a.num_seqs);
+      }
+      if (!seq_shape(it.s, it.q0, it.n, it.c)) continue;
+      if (it.t * kRows >= it.n) continue;
+      it.nkt = key_tiles(it.c, it.n, it.t);
+      return true;
+    }
+  };
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+
+  // Each role branch starts by setting its warpgroup's registers (every warp
+  // of a warpgroup takes the same setmaxnreg) and ends with the CTA-wide
+  // teardown barrier (named barrier 1, all threads).
+  auto teardown = [&]() {
+    __syncwarp();
+    tc_fence_before_sync();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  };
+
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIo));
+    if (warp == 8 || warp == 10) {
+      // --------------------------------------------- TMA producers: K (8), V (10)
+      // Each ring has its own producer, so a K tile waits only for the S
+      // products of the tile two before it and a V tile only for the PV
+      // products.  The whole warp runs the loop (one box per lane).  Pool row
+      // coordinates of an item's blocks are read 128 blocks at a time, spread
+      // over the lanes (lane l holds blocks l, l+32, l+64, l+96 of the chunk).
+      const bool is_k = warp == 8;
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      const uint32_t ring = is_k ? sK : sV;
+      const uint32_t nst = is_k ? kStagesK : kStagesV;
+      const uint64_t policy = l2_policy_evict_last();   // the other heads of the group read these tiles too
+      const int oob_row = a.num_blocks * a.num_kv_heads * kBlock;   // rows past the pool read as zero
+      uint32_t kv = 0;       // tiles issued
+      bool ok = true;
+      long long k = 0;
+      Item it;
+      auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
+      };
+      while (ok && find_item(k, it)) {
+        const int kvh = it.h / G;
+        const int nblk = it.nkt * kBlocksPerTile;
+        int yr[4];
+        int chunk = -1;
+        auto load_chunk = [&](int ch) {
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
-        if (jp < nkt_g[g])
-          ok2 = ok2 && !abort_sh &&
-                mbar_wait_bounded(is_k ? k_empty(g, jp % kStages) : v_empty(g, jp % kStages), (jp / kStages) & 1);
-      return __all_sync(0xffffffffu, ok2) != 0;
-    };
-    int next_k = 0, next_v = 0;
-    load_chunk(0);
-    for (int j = 0; j < n_kt; ++j) {
-      if (!stage_free(true, j)) {
+          for (int q = 0; q < 4; ++q) {
+            const int lb = ch * 128 + q * 32 + lane;
+            int y = oob_row;
+            if (lb < nblk && lb * kBlock < it.c) {
+              const int id = __ldg(a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq + lb);
+              if (id >= 0 && id < a.num_blocks)
+                y = (id * a.num_kv_heads + kvh) * kBlock;
+              else
+                flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            }
+            yr[q] = y;
+          }
+          chunk = ch;
+        };
+        // One box (16 rows x 128 bytes) per lane: a single issuing thread
+        // would serialise the tile's kBlocksPerTile * NBOX tensor copies.
+        auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j) {
+          const int lb0 = j * kBlocksPerTile;   // a tile's blocks never straddle a 32-block group
+          if ((lb0 >> 7) != chunk) load_chunk(lb0 >> 7);
+          const int q = (lb0 >> 5) & 3;
+          const int v = q == 0 ? yr[0] : q == 1 ? yr[1] : q == 2 ? yr[2] : yr[3];
+          const int b = lane % kBlocksPerTile;
+          const int h = lane / kBlocksPerTile;
+          const int y = __shfl_sync(0xffffffffu, v, (lb0 + b) & 31);
+          if (lane == 0) mbar_arrive_expect_tx(bar, L::KT_BYTES);
+          __syncwarp();
+          if (h < NBOX) tma_load_2d(dst + h * L::HALF_KT + b * 2048, map, h * 64, y, bar, policy);
+          __syncwarp();
+        };
+        for (int j = 0; j < it.nkt; ++j) {
+          const int st = static_cast<int>(kv % nst);
+          const uint32_t use = kv / nst;
+          // stage st is free once the products of its previous use have completed
+          if (use > 0 && !wait_all(is_k ? k_empty(st) : v_empty(st), (use - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          load_tile(map, ring + st * L::KT_BYTES, is_k ? k_full(st) : v_full(st), j);
+          ++kv;
+        }
+        ++k;
+      }
+      if (!ok) {
         abort_sh = 1;
-        break;
+        // let the copies still in flight (at most the last kStages of each
+        // ring) land before the CTA can exit
+        if (lane == 0)
+          for (uint32_t u = kv > nst ? kv - nst : 0; u < kv; ++u)
+            mbar_wait_bounded(is_k ? k_full(u % nst) : v_full(u % nst), (u / nst) & 1, 100000000ull);
       }
-      load_tile(&kmap, sK + (j % kStages) * L::KT_BYTES, k_full(j % kStages), j);
-      next_k = j + 1;
-      if (!stage_free(false, j)) {
-        abort_sh = 1;
-        break;
-      }
-      load_tile(&vmap, sV + (j % kStages) * L::KT_BYTES, v_full(j % kStages), j);
-      next_v = j + 1;
-    }
-    if (abort_sh && lane == 0) {
-      // let the copies still in flight land before the CTA can exit
-      for (int j = next_k - kStages < 0 ? 0 : next_k - kStages; j < next_k; ++j)
-        mbar_wait_bounded(k_full(j % kStages), (j / kStages) & 1, 100000000ull);
-      for (int j = next_v - kStages < 0 ? 0 : next_v - kStages; j < next_v; ++j)
-        mbar_wait_bounded(v_full(j % kStages), (j / kStages) & 1, 100000000ull);
-    }
-  } else if (warp >= 9) {
-    // ----------------------------------------------------- MMA issuer, one per tile
-    const int g = warp - 9;
-    const uint32_t tt = tmem + g * L::TMEM_TILE;
-    const uint32_t id_s = umma_idesc_f16(kRows, kKeys, kBf16, false, false);
-    const uint32_t id_o = umma_idesc_f16(kRows, D, kBf16, false, true);
-    // With one S/P buffer per tile the order is fixed -- S_0, PV_0, S_1, PV_1,
-    // ... -- so the warp blocks (suspended in mbarrier.try_wait, taking no
-    // issue slots from the softmax warps) on exactly the next input it needs.
-    bool ok = true;
-    const int my_nkt = nkt_g[g];
-    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
-    };
-    for (int j = 0; j < my_nkt && ok; ++j) {
-      const int st = j % kStages;
-      // S_j = Q K_j^T once K_j has landed and PV_{j-1} (which read P from the
-      // same columns) has completed
-      ok = wait_all(k_full(st), (j / kStages) & 1) && (j < 1 || wait_all(pv_done(g), (j - 1) & 1));
-      // Tile B starts once tile A's first softmax is done, so that the two tiles run out of
-      // phase (one tile's MMAs during the other's softmax) instead of in step on every K tile.
-      if (ok && g == 1 && j == 0) ok = wait_all(p_full(0), 0);
-      if (!ok) break;
-      tc_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t qbase = sQ + g * L::Q_BYTES;
-        const uint32_t kbase = sK + st * L::KT_BYTES;
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      // One thread issues both tiles' products in a fixed interleaved order:
+      //   S_A0 S_B0 | PV_A0 S_A1 PV_B0 S_B1 | PV_A1 S_A2 PV_B1 S_B2 | ...
+      // so the tensor pipe runs tile B's products during tile A's softmax and
+      // the other way round.  S_g(j+1) overwrites P_g(j) right after PV_g(j)
+      // has been issued: one thread's MMAs run in issue order.
+      const uint32_t id_s = umma_idesc_f16(kRows, kKeys, kBf16, false, false);
+      const uint32_t id_o = umma_idesc_f16(kRows, D, kBf16, false, true);
+      auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
+      };
+      // S_g(j) = Q_g K_j^T into tile g's S columns (lane 0 issues)
+      auto issue_s = [&](int g, int st) {
+        tc_fence_after_sync();
+        if (lane == 0) {
+          const uint32_t qbase = sQ + g * L::Q_BYTES;
+          const uint32_t kbase = sK + st * L::KT_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t da = umma_desc_sw128(qbase + (kk >> 2) * L::HALF_Q + (kk & 3) * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(kbase + (kk >> 2) * L::HALF_KT + (kk & 3) * 32, 16, 1024);
-          umma_f16(tt + L::TMEM_S, da, db, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t da = umma_desc_sw128(qbase + (kk >> 2) * L::HALF_Q + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = umma_desc_sw128(kbase + (kk >> 2) * L::HALF_KT + (kk & 3) * 32, 16, 1024);
+            umma_f16(tmem + g * L::TMEM_TILE + L::TMEM_S, da, db, id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(g));
         }
-        umma_commit(s_full(g));
-        umma_commit(k_empty(g, st));
-      }
-      __syncwarp();
-      // O += P_j V_j once V_j has landed and the softmax has written P_j
-      ok = wait_all(v_full(st), (j / kStages) & 1) && wait_all(p_full(g), j & 1);
-      if (!ok) break;
-      const uint32_t vbase = sV + st * L::KT_BYTES;
-      const int pb = c >> 4;
-      if ((c & 15) && pb / kBlocksPerTile == j) {
-        // value rows past the context read as zero (both issuers write the
-        // same zeros; each does it before its own PV reads the tile)
-        const int r0 = c & 15;
-        for (int idx = lane; idx < (16 - r0) * NBOX * 8; idx += 32) {
-          const int row = (pb % kBlocksPerTile) * 16 + r0 + idx / (NBOX * 8);
-          const int rem = idx % (NBOX * 8);
-          const uint32_t addr = vbase + (rem >> 3) * L::HALF_KT + row * 128 + ((rem & 7) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
-        }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      tc_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t ptm = tt + L::TMEM_S;   // P: kKeys/2 columns of packed pairs
+        __syncwarp();
+      };
+      // O_g += P_g(j) V_j (lane 0 issues)
+      auto issue_pv = [&](int g, int st, int j) {
+        tc_fence_after_sync();
+        if (lane == 0) {
+          const uint32_t vbase = sV + st * L::KT_BYTES;
+          const uint32_t tt = tmem + g * L::TMEM_TILE;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t db = umma_desc_sw128(vbase + kk * 2048, L::HALF_KT, 1024);
-          umma_f16_tmem_a(tt + L::TMEM_O, ptm + kk * 8, db, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t db = umma_desc_sw128(vbase + kk * 2048, L::HALF_KT, 1024);
+            umma_f16_tmem_a(tt + L::TMEM_O, tt + L::TMEM_S + kk * 8, db, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(pv_done(g));
         }
-        umma_commit(pv_done(g));
-        umma_commit(v_empty(g, st));
+        __syncwarp();
+      };
+      auto commit = [&](uint32_t bar) {
+        if (lane == 0) umma_commit(bar);
+        __syncwarp();
+      };
+      uint32_t kv = 0, tc = 0, itc = 0;   // K/V uses, tiles, items
+      bool ok = true;
+      long long k = 0;
+      Item it;
+      while (ok && find_item(k, it)) {
+        // S of the item's first K tile for each tile, once its queries are in
+        int st = static_cast<int>(kv % kStagesK);
+        ok = wait_all(k_full(st), (kv / kStagesK) & 1);
+        for (int g = 0; g < NT && ok; ++g) {
+          if (!(ok = wait_all(q_full(g), itc & 1))) break;
+          issue_s(g, st);
+          if (it.nkt == 1) commit(q_empty(g));   // the tile's last read of its queries
+        }
+        if (!ok) break;
+        commit(k_empty(st));
+        for (int j = 0; j < it.nkt; ++j, ++kv, ++tc) {
+          const int sv = static_cast<int>(kv % kStagesV);
+          const bool more = j + 1 < it.nkt;
+          const int st1 = static_cast<int>((kv + 1) % kStagesK);
+          if (!(ok = wait_all(v_full(sv), (kv / kStagesV) & 1))) break;
+          const int pb = it.c >> 4;
+          if ((it.c & 15) && pb / kBlocksPerTile == j) {
+            // value rows past the context read as zero
+            const uint32_t vbase = sV + sv * L::KT_BYTES;
+            const int r0 = it.c & 15;
+            for (int idx = lane; idx < (16 - r0) * NBOX * 8; idx += 32) {
+              const int row = (pb % kBlocksPerTile) * 16 + r0 + idx / (NBOX * 8);
+              const int rem = idx % (NBOX * 8);
+              const uint32_t addr = vbase + (rem >> 3) * L::HALF_KT + row * 128 + ((rem & 7) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          for (int g = 0; g < NT; ++g) {
+            // O_g += P_g(j) V_j once the softmax has written P_g(j); the item's
+            // first PV overwrites O_g, which the epilogue must have read
+            if (!(ok = wait_all(p_full(g), tc & 1) && (j > 0 || itc == 0 || wait_all(o_free(g), (itc - 1) & 1))))
+              break;
+            issue_pv(g, sv, j);
+            if (more) {
+              if (g == 0 && !(ok = wait_all(k_full(st1), ((kv + 1) / kStagesK) & 1))) break;
+              issue_s(g, st1);
+              if (j + 2 == it.nkt) commit(q_empty(g));   // S_g of the last K tile: last read of Q_g
+            }
+          }
+          if (!ok) break;
+          commit(v_empty(sv));
+          if (more) commit(k_empty(st1));
+        }
+        ++itc;
+        ++k;
       }
-      __syncwarp();
+      if (!ok) abort_sh = 1;
+      // every MMA issued by this warp has completed before the CTA tears down
+      commit(mma_final(0));
+      mbar_wait_bounded(mma_final(0), 0, 100000000ull);
+    } else if (warp == 11) {
+      // ---------------------------------------------------------- query loader
+      // Q rows of the item's tiles -> shared memory in the 128-byte-swizzled
+      // K-major layout: a whole tile by TMA (the 3-D query map), the prompt's
+      // last partial tile by cp.async with the rows past the prompt zeroed.
+      constexpr int CH = D / 8;   // 16-byte chunks per row
+      const uint64_t policy_q = l2_policy_evict_first();   // each query tile is read once
+      bool ok = true;
+      uint32_t itc = 0;
+      long long k = 0;
+      Item it;
+      while (ok && find_item(k, it)) {
+        for (int g = 0; g < NT && ok; ++g) {
+          // the previous item's S products of this tile (its last reads of
+          // Q_g) have completed
+          if (itc > 0) {
+            ok = !abort_sh && mbar_wait_bounded(q_empty(g), (itc - 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t qbase = sQ + g * L::Q_BYTES;
+          if ((it.t + 1) * kRows <= it.n) {
+            // a whole tile: NBOX boxes of 128 rows x 64 columns, by TMA
+            if (lane == 0) {
+              mbar_arrive_expect_tx(q_full(g), L::Q_BYTES);
+              for (int h = 0; h < NBOX; ++h)
+                tma_load_3d(qbase + h * L::HALF_Q, &qmap, h * 64, it.h + g, it.q0 + it.t * kRows, q_full(g),
+                            policy_q);
+            }
+            __syncwarp();
+          } else {
+            // the prompt's last, partial tile (whose rows past the prompt may
+            // lie past the caller's buffer): cp.async of the rows that exist
+            const T* qh = static_cast<const T*>(a.q) + static_cast<size_t>(it.h + g) * D;
+            for (int idx = lane; idx < kRows * CH; idx += 32) {
+              const int r = idx / CH;
+              const int cc = idx - r * CH;
+              const int lr = it.t * kRows + r;
+              const bool in = lr < it.n;
+              const T* src = in ? qh + (static_cast<size_t>(it.q0) + lr) * H * D + cc * 8 : qh;
+              const uint32_t dst = qbase + (cc >> 3) * L::HALF_Q + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+              cp_async_16(dst, src, in ? 16u : 0u);
+            }
+            cp_async_wait_all();
+            fence_proxy_async_smem();   // the MMAs (async proxy) read what these copies wrote
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full(g));
+          }
+        }
+        if (!ok) break;
+        ++itc;
+        ++k;
+      }
+      if (!ok) abort_sh = 1;
     }
-    if (!ok) abort_sh = 1;
-    // every MMA issued by this warp has completed before the CTA tears down
-    if (lane == 0) umma_commit(mma_final(g));
-    mbar_wait_bounded(mma_final(g), 0, 100000000ull);
-  } else {
-    // ----------------------------------------------------------- softmax warps
+    teardown();
+  } else if (warp < 4 || paired) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    // ------------------------------------------------- softmax + epilogue of tile g
     const int g = warp >> 2;
-    const int r = threadIdx.x & 127;
-    const int qr0 = (2 * pt + g) * kRows;
-    const int lr = qr0 + r;
-    const int pos = c - n + lr;                       // causal limit of this row
-    const int my_nkt = nkt_g[g];
+    const int r = threadIdx.x & 127;   // query row of the tile (tensor-memory lane)
     const uint32_t tt = tmem + g * L::TMEM_TILE;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tt + L::TMEM_O + lane_base;
-    float m_used = -INFINITY;   // reference max of this row (log2 domain)
-    float l = 0.f;              // sum of 2^(x - m_used)
-    bool ok = true;
+    const uint32_t tbuf = tt + L::TMEM_S + lane_base;
     // scale > 0 (the usual case): the max is taken on the raw scores and the
     // scale folds into one FMA per element; otherwise scale first.
     const bool pos_scale = a.scale_log2 > 0.f;
-    const int warp_pos_min = c - n + qr0 + (warp & 3) * 32;   // smallest causal limit in this warp
-    const uint32_t tbuf = tt + L::TMEM_S + lane_base;
     const float sc = pos_scale ? a.scale_log2 : 1.f;   // p = 2^(x*sc - mu) on raw scores x
-    for (int j = 0; j < my_nkt; ++j) {
-      ok = !abort_sh && mbar_wait_bounded(s_full(g), j & 1);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const int key0 = j * kKeys;
-      const bool diag = key0 + kKeys - 1 > warp_pos_min;   // a tile on the diagonal: causal mask
-      // the whole row of S in one tensor-memory load
-      float x[kKeys];
-      tmem_ld128(tbuf, x);
-      if (!pos_scale) {
-#pragma unroll
-        for (int i = 0; i < kKeys; ++i) x[i] *= a.scale_log2;
-      }
-      if (diag) {
-#pragma unroll
-        for (int i = 0; i < kKeys; ++i)
-          if (key0 + i > pos) x[i] = -INFINITY;
-      }
-      float pm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = x[k];
-#pragma unroll
-      for (int i = 8; i < kKeys; i += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], x[i + k]);
-      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      if (pos_scale) mx *= a.scale_log2;
-      const bool need = mx > m_used + 8.f;
-      float factor = 1.f;
-      if (need) {
-        factor = exp2f(m_used - mx);   // 0 when m_used is still -inf
-        l *= factor;
-        m_used = mx;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // rescale this warp's rows of O; PV_{j-1} has completed (S_j waited for it)
-        ok = mbar_wait_bounded(pv_done(g), (j - 1) & 1);
+    uint32_t tc = 0;
+    bool ok = true;
+    long long k = 0;
+    Item it;
+    while (ok && find_item(k, it)) {
+      const int pos = it.c - it.n + it.t * kRows + r;                    // causal limit of this row
+      const int warp_pos_min = it.c - it.n + it.t * kRows + (warp & 3) * 32;
+      float m_used = -INFINITY;   // reference max of this row (log2 domain)
+      float l = 0.f;              // sum of 2^(x - m_used)
+      for (int j = 0; j < it.nkt; ++j, ++tc) {
+        ok = !abort_sh && mbar_wait_bounded(s_full(g), tc & 1);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
+        const int key0 = j * kKeys;
+        const bool diag = key0 + kKeys - 1 > warp_pos_min;   // a tile on the diagonal: causal mask
+        float x[kKeys];
+        tmem_ld128(tbuf, x);
+        if (!pos_scale) {
+#pragma unroll
+          for (int i = 0; i < kKeys; ++i) x[i] *= a.scale_log2;
+        }
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < kKeys; ++i)
+            if (key0 + i > pos) x[i] = -INFINITY;
+        }
+        float pm[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pm[q] = x[q];
+#pragma unroll
+        for (int i = 8; i < kKeys; i += 8)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) pm[q] = fmaxf(pm[q], x[i + q]);
+        float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                         fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        if (pos_scale) mx *= a.scale_log2;
+        const bool need = mx > m_used + 8.f;
+        float factor = 1.f;
+        if (need) {
+          factor = exp2f(m_used - mx);   // 0 when m_used is still -inf
+          l *= factor;
+          m_used = mx;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // rescale this warp's rows of O once the previous tile's PV has completed
+          ok = !abort_sh && mbar_wait_bounded(pv_done(g), (tc - 1) & 1);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
 #pragma unroll 1
-        for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: the row of S is still live
-          float o[16];
-          tmem_ld16(tO + cc * 16, o);
-          uint32_t ob[16];
+          for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: the row of S is still live
+            float o[16];
+            tmem_ld16(tO + cc * 16, o);
+            uint32_t ob[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ob[i] = __float_as_uint(o[i] * factor);
-          tmem_st16_u(tO + cc * 16, ob);
-        }
-      }
-      const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = 2^(x - mu), packed two per column over the front of S
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
-#pragma unroll
-      for (int cc = 0; cc < kKeys / 32; ++cc) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(fmaf(x[cc * 32 + 2 * i], sc, -mu));
-          const float p1 = fast_exp2(fmaf(x[cc * 32 + 2 * i + 1], sc, -mu));
-          ps[(2 * i) & 7] += p0;
-          ps[(2 * i + 1) & 7] += p1;
-          w[i] = Mma<T>::pack(p0, p1);
-        }
-        tmem_st16_u(tbuf + cc * 16, w);   // keys 32cc+2i, 32cc+2i+1 in column 16cc+i
-      }
-      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(g));
-    }
-    if (!ok) {
-      abort_sh = 1;
-    } else if (my_nkt > 0) {
-      // the last PV (and so every PV before it) has completed
-      ok = mbar_wait_bounded(pv_done(g), (my_nkt - 1) & 1);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after_sync();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        T* orow = static_cast<T*>(a.out) + ((static_cast<size_t>(q0) + lr) * a.num_q_heads + hq) * D;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO + cc * 32, o);
-          if (lr < n) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint4 v;
-              v.x = Mma<T>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
-              v.y = Mma<T>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
-              v.z = Mma<T>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
-              v.w = Mma<T>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
-              reinterpret_cast<uint4*>(orow + cc * 32)[e] = v;
-            }
+            for (int i = 0; i < 16; ++i) ob[i] = __float_as_uint(o[i] * factor);
+            tmem_st16_u(tO + cc * 16, ob);
           }
         }
-      } else {
-        abort_sh = 1;
+        const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+        // P = 2^(x - mu), packed two per column over the front of S
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
+#pragma unroll
+        for (int cc = 0; cc < kKeys / 32; ++cc) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = fast_exp2(fmaf(x[cc * 32 + 2 * i], sc, -mu));
+            const float p1 = fast_exp2(fmaf(x[cc * 32 + 2 * i + 1], sc, -mu));
+            ps[(2 * i) & 7] += p0;
+            ps[(2 * i + 1) & 7] += p1;
+            w[i] = Mma<T>::pack(p0, p1);
+          }
+          tmem_st16_u(tbuf + cc * 16, w);   // keys 32cc+2i, 32cc+2i+1 in column 16cc+i
+        }
+        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(g));
       }
+      if (!ok) break;
+      // epilogue: once the item's last PV has completed, O / l -> out
+      ok = !abort_sh && mbar_wait_bounded(pv_done(g), (tc - 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int lr = it.t * kRows + r;
+      T* orow = static_cast<T*>(a.out) + ((static_cast<size_t>(it.q0) + lr) * H + it.h + g) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tO + cc * 32, o);
+        if (lr < it.n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 v;
+            v.x = Mma<T>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
+            v.y = Mma<T>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
+            v.z = Mma<T>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
+            v.w = Mma<T>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
+            reinterpret_cast<uint4*>(orow + cc * 32)[e] = v;
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free(g));
+      ++k;
     }
-  }
-
-  // ------------------------------------------------------------------ teardown
-  tc_fence_before_sync();
-  __syncthreads();
-  if (threadIdx.x == 0 && abort_sh) flag_status(a.status, PA_DEV_WAIT_TIMEOUT);
-  if (warp == 0) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    if (!ok) abort_sh = 1;
+    teardown();
+    if (threadIdx.x == 0 && abort_sh) flag_status(a.status, PA_DEV_WAIT_TIMEOUT);
+    if (warp == 0) {
+      tc_fence_after_sync();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+  } else {
+    // tile B's softmax warps when the query group is odd (no tile B): idle
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    teardown();
   }
 }
 
 namespace {
 template <typename T, int D>
 cudaError_t launch_umma_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream) {
+                          const CUtensorMap& qmap, cudaStream_t stream) {
   const int smem = UmmaLayout<D>::SMEM + 1024;
   auto kern = prefill_umma_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long n_pairs = ((a.max_q_len + kRows - 1) / kRows + 1) / 2;
-  const long long ctas = n_pairs * a.num_q_heads * a.num_seqs;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, kmap, vmap, a);
+  // persistent: one CTA per SM, or fewer when there are fewer items
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 152;
+  const int nt = (a.num_q_heads / a.num_kv_heads) % 2 == 0 ? 2 : 1;
+  const long long items = static_cast<long long>((a.max_q_len + kRows - 1) / kRows) * (a.num_q_heads / nt) *
+                          a.num_seqs;
+  const long long ctas = items < sms ? items : sms;
+  if (ctas <= 0) return cudaSuccess;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, kmap, vmap, qmap, a);
 }
 }  // namespace
 
 cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, cudaStream_t stream) {
+                                const CUtensorMap& vmap, const CUtensorMap& qmap, cudaStream_t stream) {
   if (dtype == PA_BF16) {
-    return a.head_dim == 128 ? launch_umma_t<__nv_bfloat16, 128>(a, kmap, vmap, stream)
-                             : launch_umma_t<__nv_bfloat16, 64>(a, kmap, vmap, stream);
+    return a.head_dim == 128 ? launch_umma_t<__nv_bfloat16, 128>(a, kmap, vmap, qmap, stream)
+                             : launch_umma_t<__nv_bfloat16, 64>(a, kmap, vmap, qmap, stream);
   }
-  return a.head_dim == 128 ? launch_umma_t<__half, 128>(a, kmap, vmap, stream)
-                           : launch_umma_t<__half, 64>(a, kmap, vmap, stream);
+  return a.head_dim == 128 ? launch_umma_t<__half, 128>(a, kmap, vmap, qmap, stream)
+                           : launch_umma_t<__half, 64>(a, kmap, vmap, qmap, stream);
 }
 
 }  // namespace pa
