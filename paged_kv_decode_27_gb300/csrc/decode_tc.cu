@@ -66,10 +66,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const int G = a.num_q_heads / a.num_kv_heads;
 
   grid_dependency_wait();   // inputs may come from the kernel just before us
-  // The next kernel launched with programmatic serialisation (a decode of the
-  // next layer, say) may be scheduled once every CTA of this grid is running;
-  // it waits for this grid's completion before it reads or writes anything.
-  allow_dependents();
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
