@@ -617,7 +617,9 @@ def run_ours(args, rank, world, local_rank):
 # Layers of the model each workload's head shape comes from (attention-only
 # per-model figures divide the one-layer rate by this).
 N_LAYERS = {"tiny_fp32": 1, "llama32_1b_decode": 16, "llama3_8b_decode": 32, "prefix_shared_8k": 32,
-            "mixed_mistral7b": 32, "llama3_8b_long_b1": 32, "llama3_8b_long_b4": 32}
+            "mixed_mistral7b": 32, "llama3_8b_long_b1": 32, "llama3_8b_long_b4": 32,
+            "llama32_1b_decode_int8": 16, "llama3_8b_decode_int8": 32, "llama3_8b_verify": 32,
+            "llama3_8b_verify_int8": 32, "llama3_8b_decode_rope": 32}
 # The five configurations of the benchmark's workload list, then the small-batch
 # end of its decode range (batch 1 and 4 at contexts up to 8192).
 CONFIGS = ["tiny_fp32", "llama32_1b_decode", "llama3_8b_decode", "prefix_shared_8k", "mixed_mistral7b",
@@ -741,7 +743,8 @@ def measure_workload(name, pa, W, torch, dev, reps, warmup, partition=0, flush=N
     tok_s = S / ((med["append"] + med["decode"] + med["prefill"]) * 1e-6)
     line = {"workload": wl.name, "description": wl.description, "reps": reps, "warmup": warmup,
             "l2": "evicted before every repetition (a read of 2x the L2 size)",
-            "partition_tokens": pa.pa_decode_partition_size(S, max_ctx, kp, partition),
+            # the decode's partition (a verification pass chooses its own split)
+            "partition_tokens": None if vq else pa.pa_decode_partition_size(S, max_ctx, kp, partition),
             "append_us": med["append"], "append_p90_us": p90["append"],
             "append_gbs": wl.append_bytes() / (med["append"] * 1e-6) / 1e9,
             "attention_us": med["decode"], "attention_p90_us": p90["decode"],

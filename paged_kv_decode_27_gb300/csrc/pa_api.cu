@@ -115,17 +115,20 @@ int current_sms() {
   return n > 0 ? n : kDefaultSms;
 }
 
-int choose_partition_on(int num_seqs, int num_kv_heads, int max_context_len, int requested, int sms) {
+// ctas_per_sm: CTAs of the kernel resident on one SM; past_wave: the
+// partition when not even 2048-token partitions fit one wave.
+int choose_partition_on(int num_seqs, int num_kv_heads, int max_context_len, int requested, int sms,
+                        int ctas_per_sm = kCtasPerSm, int past_wave = 1024) {
   if (requested > 0) return requested;
   // One resident wave when the batch allows it: the largest partition count
   // (smallest partition, not below kMinPartition) whose (sequence, KV head,
   // partition) units all fit on the GPU at once.  Past that the decode runs in
-  // several waves of 1024-token partitions.
-  const long long wave = static_cast<long long>(kCtasPerSm) * (sms > 0 ? sms : kDefaultSms);
+  // several waves of past_wave-token partitions.
+  const long long wave = static_cast<long long>(ctas_per_sm) * (sms > 0 ? sms : kDefaultSms);
   const auto units = [&](int p) {
     return static_cast<long long>(num_seqs) * num_kv_heads * ((max_context_len + p - 1) / p);
   };
-  if (units(kMaxPartition) > wave) return 1024;
+  if (units(kMaxPartition) > wave) return past_wave;
   int p = kMaxPartition;
   while (p > kMinPartition && units(p / 2) <= wave) p /= 2;
   return p;
@@ -134,6 +137,24 @@ int choose_partition_on(int num_seqs, int num_kv_heads, int max_context_len, int
 int choose_partition(int num_seqs, int num_kv_heads, int max_context_len, int requested) {
   return choose_partition_on(num_seqs, num_kv_heads, max_context_len, requested,
                              requested > 0 ? kDefaultSms : current_sms());
+}
+
+// The INT8 kernel with more than one 8-column query tile (a verification pass
+// of G * q_len > 8 query columns) holds more accumulators: 2 CTAs per SM, and
+// each CTA pays a fixed start-up (its query tiles widened and scaled, their
+// bias products, a merge of every column), so when the batch does not fit one
+// wave it takes the longest partitions (measured on the Llama-3-8B-shaped
+// batch-64 pass of 4 drafts: 471 / 307 / 225 / 194 us at 256 / 512 / 1024 /
+// 2048 tokens).
+bool int8_wide(int num_q_heads, int q_len, const pa_pool_desc* pool) {
+  return pool->dtype == PA_I8 && q_len > 1 && (num_q_heads / pool->num_kv_heads) * q_len > 8;
+}
+
+int choose_partition_for(int num_seqs, int num_q_heads, int q_len, int max_context_len, int requested,
+                         const pa_pool_desc* pool) {
+  if (!int8_wide(num_q_heads, q_len, pool)) return choose_partition(num_seqs, pool->num_kv_heads, max_context_len, requested);
+  return choose_partition_on(num_seqs, pool->num_kv_heads, max_context_len, requested,
+                             requested > 0 ? kDefaultSms : current_sms(), 2, kMaxPartition);
 }
 
 int max_splits_for(int max_context_len, int part_blocks) {
@@ -497,7 +518,7 @@ size_t pa_verify_workspace_size(int num_seqs, int q_len, int num_q_heads, int ma
     fail(PA_ERR_INVALID, "q_len must be >= 1");
     return 0;
   }
-  const int p = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int p = choose_partition_for(num_seqs, num_q_heads, q_len, max_context_len, partition_size, pool);
   const int ms = verify_slots(q_len, pool, max_context_len, p / PA_BLOCK_SIZE);
   return ws_layout(num_seqs * q_len, num_q_heads, ms, pool->head_dim).total;
 }
@@ -675,7 +696,7 @@ int int8_attention(void* out, const void* q, const void* k_codes, const void* v_
   if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return fail(PA_ERR_INVALID, "block_tables and context_lens must be 4-byte aligned");
 
-  const int part = choose_partition(num_seqs, pool->num_kv_heads, max_context_len, partition_size);
+  const int part = choose_partition_for(num_seqs, num_q_heads, q_len, max_context_len, partition_size, pool);
   const int part_blocks = part / PA_BLOCK_SIZE;
   const int max_splits = max_splits_for(max_context_len, part_blocks);
   const WsLayout ws = ws_layout(num_seqs * q_len, num_q_heads, max_splits, pool->head_dim);

@@ -216,6 +216,16 @@ def test_int8_verify_validates_on_the_host(lib):
     for S, ql, maxc, part in ((64, 5, 8224, 512), (3, 2, 4000, 256), (8, 8, 100, 16)):
         assert lib.pa_verify_workspace_size(S, ql, 32, maxc, part, ctypes.byref(d8)) == \
             lib.pa_decode_workspace_size(S * ql, 32, maxc, part, ctypes.byref(d8))
+    # The automatic partition of a wide INT8 verification pass (G x q_len > 8
+    # query columns: 2 CTAs per SM) fills one wave of 2 x 152 CTAs when it can
+    # (1 sequence x 8 KV heads x 33 partitions of 256 tokens = 264) and
+    # otherwise takes 2048-token partitions (the batch of 64: 2560 units).
+    auto = lambda S, ql, maxc: lib.pa_verify_workspace_size(S, ql, 32, maxc, 0, ctypes.byref(d8))
+    assert auto(64, 5, 8224) == lib.pa_decode_workspace_size(64 * 5, 32, 8224, 2048, ctypes.byref(d8))
+    assert auto(1, 5, 8192) == lib.pa_decode_workspace_size(5, 32, 8192, 256, ctypes.byref(d8))
+    # two query columns per KV head (one 8-column tile) keep the decode rule
+    assert lib.pa_verify_workspace_size(64, 2, 8, 8224, 0, ctypes.byref(d8)) == \
+        lib.pa_decode_workspace_size(64 * 2, 8, 8224, 1024, ctypes.byref(d8))
 
 
 def test_int8_without_gpu_is_a_cuda_error(lib):
