@@ -83,8 +83,10 @@ def test_verify_q_len_1_is_decode_bit_for_bit():
 
 
 def test_verify_rows_match_decode_at_each_position():
-    """Row i of a verification pass equals a decode of the same query with the
-    context cut at its position (two GPU paths, within the bf16 bar)."""
+    """Consistency check, not parity evidence (both sides are GPU paths): row i
+    of a verification pass equals a decode of the same query with the context
+    cut at its position, within the bf16 bar.  Parity of each path against the
+    oracle is tested separately."""
     wl = W.small_random(99, 3, 0, 32, 8, 128, torch.bfloat16, ctx=[40, 130, 700])
     ctx = torch.tensor([40, 130, 700], dtype=torch.int32)
     q = wl.verify_queries(0, 5)
