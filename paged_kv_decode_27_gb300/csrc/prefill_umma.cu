@@ -32,10 +32,17 @@
 // products run during the other's softmax.  It issues S for K tile j + 1
 // right after PV for tile j: the MMAs of one thread run in issue order, so
 // S_{j+1} overwrites the columns of P_j only after PV_j has read them, and
-// the next S needs no wait on the PV's completion.
+// the next S needs no wait on the PV's completion.  The same order makes the
+// completion of S_g(j) imply that of every product issued before it (PV of
+// both tiles for K tile j - 1), so the softmax needs no separate signal for
+// the previous PV and hands the K and V stages back to the producers itself.
+// The tensor core accepts barely more than one MMA ahead of the one it runs,
+// so every wait or branch of the issuing thread between two products leaves
+// the pipe idle: the issuer is one thread with precomputed descriptors and
+// two commits per K tile (S of each tile).
 //
 // Tensor memory (512 columns): per tile S/P (128 columns) and O (D columns).
-// Shared memory: Q_A, Q_B, a 2-stage K ring and a 2-stage V ring, the sorted
+// Shared memory: Q_A, Q_B, a 2-stage K ring and a 3-stage V ring, the sorted
 // work list.
 //
 // Warps (384 threads, three warpgroups that re-balance their registers with
@@ -44,7 +51,7 @@
 //              end of an item the epilogue: normalise O and store the rows;
 //   8 / 10     TMA producers of the K ring / the V ring (pool rows through the
 //              block table);
-//   9          MMA issuer of both tiles (one elected lane), in the interleaved
+//   9          MMA issuer of both tiles (lane 0 alone), in the interleaved
 //              order below;
 //   11         query loader: the next item's Q tiles (TMA; cp.async for a
 //              prompt's last partial tile), once the current item's S
@@ -159,7 +166,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesK; ++i) {
       mbar_init(k_full(i), 1);
-      mbar_init(k_empty(i), 1);   // released once every product reading the stage has completed
+      mbar_init(k_empty(i), 1);   // released by the last tile's softmax once the S products of the tile have completed
     }
     for (int i = 0; i < kStagesV; ++i) {
       mbar_init(v_full(i), 1);
@@ -297,7 +304,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // --------------------------------------------- TMA producers: K (8), V (10)
       // Each ring has its own producer, so a K tile waits only for the S
       // products of the tile two before it and a V tile only for the PV
-      // products.  The whole warp runs the loop (one box per lane).  Pool row
+      // products (the last tile's softmax releases both, see the issuer).  The whole warp runs the loop (one box per lane).  Pool row
       // coordinates of an item's blocks are read 128 blocks at a time, spread
       // over the lanes (lane l holds blocks l, l+32, l+64, l+96 of the chunk).
       const bool is_k = warp == 8;
@@ -372,108 +379,95 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       }
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
-      // One thread issues both tiles' products in a fixed interleaved order:
+      // One thread (lane 0) issues both tiles' products in a fixed interleaved order:
       //   S_A0 S_B0 | PV_A0 S_A1 PV_B0 S_B1 | PV_A1 S_A2 PV_B1 S_B2 | ...
-      // so the tensor pipe runs tile B's products during tile A's softmax and
-      // the other way round.  S_g(j+1) overwrites P_g(j) right after PV_g(j)
-      // has been issued: one thread's MMAs run in issue order.
-      const uint32_t id_s = umma_idesc_f16(kRows, kKeys, kBf16, false, false);
-      const uint32_t id_o = umma_idesc_f16(kRows, D, kBf16, false, true);
-      auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
-      };
-      // S_g(j) = Q_g K_j^T into tile g's S columns (lane 0 issues)
-      auto issue_s = [&](int g, int st) {
-        tc_fence_after_sync();
-        if (lane == 0) {
-          const uint32_t qbase = sQ + g * L::Q_BYTES;
-          const uint32_t kbase = sK + st * L::KT_BYTES;
+      if (lane == 0) {
+        const uint32_t id_s = umma_idesc_f16(kRows, kKeys, kBf16, false, false);
+        const uint32_t id_o = umma_idesc_f16(kRows, D, kBf16, false, true);
+        // a wait whose phase has already completed costs one try_wait; the abort
+        // flag is read only when the wait has to block
+        auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
+          return mbar_try_wait(bar, parity) || (!abort_sh && mbar_wait_bounded(bar, parity));
+        };
+        // descriptors of the operand bases; the start address field (bits 0-13,
+        // 16-byte units) takes the in-tile offsets by plain addition
+        const uint64_t dq = umma_desc_sw128(sQ, 16, 1024);
+        const uint64_t dk = umma_desc_sw128(sK, 16, 1024);
+        const uint64_t dv = umma_desc_sw128(sV, L::HALF_KT, 1024);
+        auto issue_s = [&](int g, int st) {
+          tc_fence_after_sync();
+          const uint64_t ba = dq + static_cast<uint64_t>((g * L::Q_BYTES) >> 4);
+          const uint64_t bb = dk + static_cast<uint64_t>((st * L::KT_BYTES) >> 4);
+          const uint32_t td = tmem + g * L::TMEM_TILE + L::TMEM_S;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t da = umma_desc_sw128(qbase + (kk >> 2) * L::HALF_Q + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = umma_desc_sw128(kbase + (kk >> 2) * L::HALF_KT + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + g * L::TMEM_TILE + L::TMEM_S, da, db, id_s, kk > 0 ? 1u : 0u);
+            umma_f16(td, ba + static_cast<uint64_t>(((kk >> 2) * L::HALF_Q + (kk & 3) * 32) >> 4),
+                     bb + static_cast<uint64_t>(((kk >> 2) * L::HALF_KT + (kk & 3) * 32) >> 4), id_s, kk > 0 ? 1u : 0u);
           }
           umma_commit(s_full(g));
-        }
-        __syncwarp();
-      };
-      // O_g += P_g(j) V_j (lane 0 issues)
-      auto issue_pv = [&](int g, int st, int j) {
-        tc_fence_after_sync();
-        if (lane == 0) {
-          const uint32_t vbase = sV + st * L::KT_BYTES;
+        };
+        auto issue_pv = [&](int g, int st, int j, bool last) {
+          tc_fence_after_sync();
+          const uint64_t bb = dv + static_cast<uint64_t>((st * L::KT_BYTES) >> 4);
           const uint32_t tt = tmem + g * L::TMEM_TILE;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t db = umma_desc_sw128(vbase + kk * 2048, L::HALF_KT, 1024);
-            umma_f16_tmem_a(tt + L::TMEM_O, tt + L::TMEM_S + kk * 8, db, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_f16_tmem_a(tt + L::TMEM_O, tt + L::TMEM_S + kk * 8, bb + static_cast<uint64_t>((kk * 2048) >> 4), id_o,
+                            (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(pv_done(g));
-        }
-        __syncwarp();
-      };
-      auto commit = [&](uint32_t bar) {
-        if (lane == 0) umma_commit(bar);
-        __syncwarp();
-      };
-      uint32_t kv = 0, tc = 0, itc = 0;   // K/V uses, tiles, items
-      bool ok = true;
-      long long k = 0;
-      Item it;
-      while (ok && find_item(k, it)) {
-        // S of the item's first K tile for each tile, once its queries are in
-        int st = static_cast<int>(kv % kStagesK);
-        ok = wait_all(k_full(st), (kv / kStagesK) & 1);
-        for (int g = 0; g < NT && ok; ++g) {
-          if (!(ok = wait_all(q_full(g), itc & 1))) break;
-          issue_s(g, st);
-          if (it.nkt == 1) commit(q_empty(g));   // the tile's last read of its queries
-        }
-        if (!ok) break;
-        commit(k_empty(st));
-        for (int j = 0; j < it.nkt; ++j, ++kv, ++tc) {
-          const int sv = static_cast<int>(kv % kStagesV);
-          const bool more = j + 1 < it.nkt;
-          const int st1 = static_cast<int>((kv + 1) % kStagesK);
-          if (!(ok = wait_all(v_full(sv), (kv / kStagesV) & 1))) break;
-          const int pb = it.c >> 4;
-          if ((it.c & 15) && pb / kBlocksPerTile == j) {
-            // value rows past the context read as zero
-            const uint32_t vbase = sV + sv * L::KT_BYTES;
-            const int r0 = it.c & 15;
-            for (int idx = lane; idx < (16 - r0) * NBOX * 8; idx += 32) {
-              const int row = (pb % kBlocksPerTile) * 16 + r0 + idx / (NBOX * 8);
-              const int rem = idx % (NBOX * 8);
-              const uint32_t addr = vbase + (rem >> 3) * L::HALF_KT + row * 128 + ((rem & 7) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          for (int g = 0; g < NT; ++g) {
-            // O_g += P_g(j) V_j once the softmax has written P_g(j); the item's
-            // first PV overwrites O_g, which the epilogue must have read
-            if (!(ok = wait_all(p_full(g), tc & 1) && (j > 0 || itc == 0 || wait_all(o_free(g), (itc - 1) & 1))))
-              break;
-            issue_pv(g, sv, j);
-            if (more) {
-              if (g == 0 && !(ok = wait_all(k_full(st1), ((kv + 1) / kStagesK) & 1))) break;
-              issue_s(g, st1);
-              if (j + 2 == it.nkt) commit(q_empty(g));   // S_g of the last K tile: last read of Q_g
-            }
+          if (last) umma_commit(pv_done(g));   // the epilogue's wait: the item's last PV of tile g
+        };
+        uint32_t tc = 0, itc = 0;   // steps, items
+        int sk = 0, sv = 0;           // K / V ring stages of the next tile
+        uint32_t pk = 0, pv = 0;      // and the phase parity of their full barriers
+        bool ok = true;
+        long long k = 0;
+        Item it;
+        while (ok && find_item(k, it)) {
+          ok = wait1(k_full(sk), pk);
+          for (int g = 0; g < NT && ok; ++g) {
+            if (!(ok = wait1(q_full(g), itc & 1))) break;
+            issue_s(g, sk);
+            if (it.nkt == 1) umma_commit(q_empty(g));
           }
           if (!ok) break;
-          commit(v_empty(sv));
-          if (more) commit(k_empty(st1));
+          for (int j = 0; j < it.nkt; ++j, ++tc) {
+            const bool more = j + 1 < it.nkt;
+            if (++sk == kStagesK) { sk = 0; pk ^= 1u; }   // K tile j + 1 (the next item's first after the last)
+            if (!(ok = wait1(v_full(sv), pv))) break;
+            const int pb = it.c >> 4;
+            if ((it.c & 15) && pb / kBlocksPerTile == j) {
+              const uint32_t vbase = sV + sv * L::KT_BYTES;
+              const int r0 = it.c & 15;
+              for (int idx = 0; idx < (16 - r0) * NBOX * 8; ++idx) {
+                const int row = (pb % kBlocksPerTile) * 16 + r0 + idx / (NBOX * 8);
+                const int rem = idx % (NBOX * 8);
+                const uint32_t addr = vbase + (rem >> 3) * L::HALF_KT + row * 128 + ((rem & 7) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+              }
+              fence_proxy_async_smem();
+            }
+            for (int g = 0; g < NT; ++g) {
+              if (!(ok = wait1(p_full(g), tc & 1) && (j > 0 || itc == 0 || wait1(o_free(g), (itc - 1) & 1))))
+                break;
+              issue_pv(g, sv, j, !more);
+              if (more) {
+                if (g == 0 && !(ok = wait1(k_full(sk), pk))) break;
+                issue_s(g, sk);
+                if (j + 2 == it.nkt) umma_commit(q_empty(g));
+              }
+            }
+            if (!ok) break;
+            if (++sv == kStagesV) { sv = 0; pv ^= 1u; }
+          }
+          ++itc;
+          ++k;
         }
-        ++itc;
-        ++k;
+        if (!ok) abort_sh = 1;
+        umma_commit(mma_final(0));
+        mbar_wait_bounded(mma_final(0), 0, 100000000ull);
       }
-      if (!ok) abort_sh = 1;
-      // every MMA issued by this warp has completed before the CTA tears down
-      commit(mma_final(0));
-      mbar_wait_bounded(mma_final(0), 0, 100000000ull);
+      __syncwarp();
     } else if (warp == 11) {
       // ---------------------------------------------------------- query loader
       // Q rows of the item's tiles -> shared memory in the 128-byte-swizzled
@@ -545,7 +539,12 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     // scale folds into one FMA per element; otherwise scale first.
     const bool pos_scale = a.scale_log2 > 0.f;
     const float sc = pos_scale ? a.scale_log2 : 1.f;   // p = 2^(x*sc - mu) on raw scores x
-    uint32_t tc = 0;
+    uint32_t tc = 0, itc = 0;
+    uint32_t kvc = 0;   // K/V tiles of the items before this one
+    // the last tile's softmax hands the K and V stages back to the producers:
+    // S_g(j) of the last tile completes after every earlier product of the
+    // single issuing thread (PV(j - 1) of both tiles included)
+    const bool releaser = g == NT - 1 && (warp & 3) == 0 && lane == 0;
     bool ok = true;
     long long k = 0;
     Item it;
@@ -561,6 +560,10 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           break;
         }
         tc_fence_after_sync();
+        if (releaser) {
+          mbar_arrive(k_empty(static_cast<int>((kvc + j) % kStagesK)));
+          if (j > 0) mbar_arrive(v_empty(static_cast<int>((kvc + j - 1) % kStagesV)));
+        }
         const int key0 = j * kKeys;
         const bool diag = key0 + kKeys - 1 > warp_pos_min;   // a tile on the diagonal: causal mask
         float x[kKeys];
@@ -592,13 +595,8 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           m_used = mx;
         }
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // rescale this warp's rows of O once the previous tile's PV has completed
-          ok = !abort_sh && mbar_wait_bounded(pv_done(g), (tc - 1) & 1);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
+          // rescale this warp's rows of O: PV_g(j - 1) was issued before S_g(j),
+          // so it has completed once S_g(j) has
 #pragma unroll 1
           for (int cc = 0; cc < D / 16; ++cc) {   // 16 columns at a time: the row of S is still live
             float o[16];
@@ -633,11 +631,14 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       }
       if (!ok) break;
       // epilogue: once the item's last PV has completed, O / l -> out
-      ok = !abort_sh && mbar_wait_bounded(pv_done(g), (tc - 1) & 1);
+      ok = !abort_sh && mbar_wait_bounded(pv_done(g), itc & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
+      if (releaser) mbar_arrive(v_empty(static_cast<int>((kvc + it.nkt - 1) % kStagesV)));
+      kvc += it.nkt;
+      ++itc;
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int lr = it.t * kRows + r;
