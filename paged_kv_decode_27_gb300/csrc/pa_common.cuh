@@ -508,6 +508,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 // Byte offset of element column `col` (2-byte elements) of row `row` inside a
 // TMA box of [rows][64] elements written with 128-byte swizzling: each
 // 128-byte row's 16-byte chunks are permuted by XOR with (row % 8).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completing on an mbarrier
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
   return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
 }
