@@ -38,7 +38,8 @@ def _case(seed, qlens, prior, hq=32, hkv=8, d=128, dtype=torch.bfloat16):
     ([257], [0]),
 ])
 @pytest.mark.parametrize("hq,hkv,d,dtype", [(32, 8, 128, torch.bfloat16), (8, 8, 64, torch.bfloat16),
-                                            (16, 2, 64, torch.float16)])
+                                            (16, 2, 64, torch.float16),
+                                            (12, 4, 128, torch.float16)])   # odd group: one tile per item
 def test_prefill_small(qlens, prior, hq, hkv, d, dtype):
     wl, q, cu, ctx = _case(50 + sum(qlens) + d, qlens, prior, hq, hkv, d, dtype)
     fill_unused_with_nan(wl, ctx)
