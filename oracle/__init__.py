@@ -22,6 +22,7 @@ from .kv_int8 import (  # noqa: F401,E402
     decode_int8_ref,
     dequantize_rows_int8,
     gather_dequantized,
+    prefill_int8_ref,
     quantize_rows_int8,
     verify_int8_ref,
 )

@@ -23,6 +23,9 @@ x_q = round(x / s), x_hat = s * x_q):
   Decoding*: the target model checks the K drafted tokens in one pass, q_len =
   K + 1 query tokens per sequence): query i of a sequence with context c sits
   at position c - q_len + i and attends the dequantised keys 0..that position.
+* ``prefill_int8_ref`` -- the prompt pass over the same cache ("LLM Inference
+  Server", Stage 1: all prompt tokens at once under the causal mask): the float
+  oracle's prompt pass with each sequence's K and V dequantised.
 
 Layout: codes ``int8 [num_blocks][H_kv][16][D]`` (the float pool's layout),
 scales ``float32 [num_blocks][H_kv][16]`` (one per token slot and head).
@@ -130,4 +133,32 @@ def verify_int8_ref(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray, k_s
         for i in range(q_len):
             pos = c - q_len + i
             out[s, i] = attend(q64[s, i], k, v, scale, max(pos + 1, 0))
+    return out
+
+
+def prefill_int8_ref(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray, k_scales: np.ndarray,
+                     v_scales: np.ndarray, block_tables: np.ndarray, cu_q_lens: np.ndarray,
+                     context_lens: np.ndarray, scale: float, rows=None) -> np.ndarray:
+    """q: [sum_s q_len_s][H_q][D] (bf16 bits, fp16 or fp32); sequence s owns
+    rows cu_q_lens[s] .. cu_q_lens[s+1]-1, its prompt already in the cache.
+    Query i of sequence s sits at position p = context_lens[s] - q_len_s + i
+    and attends the dequantised keys 0..p.  Returns float64 [sum q_len][H_q][D];
+    ``rows`` optionally restricts the computation to a set of global rows
+    (the others stay zero)."""
+    q64 = as_f64(q)
+    total, h_q, d = q64.shape
+    out = np.zeros((total, h_q, d), dtype=np.float64)
+    want = None if rows is None else set(int(r) for r in rows)
+    for s in range(len(context_lens)):
+        lo, hi = int(cu_q_lens[s]), int(cu_q_lens[s + 1])
+        n = hi - lo
+        c = int(context_lens[s])
+        if n == 0 or (want is not None and not any(lo <= r < hi for r in want)):
+            continue
+        k = gather_dequantized(k_codes, k_scales, block_tables[s], c)
+        v = gather_dequantized(v_codes, v_scales, block_tables[s], c)
+        for i in range(n):
+            if want is not None and (lo + i) not in want:
+                continue
+            out[lo + i] = attend(q64[lo + i], k, v, scale, max(c - n + i + 1, 0))
     return out

@@ -12,8 +12,10 @@ code and scale pools, and against the error bound that V quantisation
 implies.  The INT8 verification pass is checked against the decode oracle at
 q_len = 1, the pinned float prompt pass on exactly representable pools, a
 torch float64 masked softmax over rows walked out of the pools, and the one-key
-case of a fresh context.  The last group plants plausible mistakes and checks
-that the pins catch them.
+case of a fresh context.  The INT8 prompt pass is checked against the pinned
+float prompt pass on exactly representable pools and against the INT8
+verification pass (one sequence's whole prompt as its q_len rows).  The last
+group plants plausible mistakes and checks that the pins catch them.
 """
 from __future__ import annotations
 
@@ -340,6 +342,42 @@ def test_verify_int8_against_masked_softmax_from_pools():
             w = torch.softmax(x, dim=-1).nan_to_num(0.0)                      # all-masked rows -> 0
             want = (w @ vh[:, hh // G, :]).numpy()
             assert np.max(np.abs(got[s, :, hh, :] - want)) < 1e-12
+
+
+def test_prefill_int8_equals_float_prefill_on_exact_pools():
+    """On pools that hold x_hat = s * x_q exactly, the INT8 prompt pass is the
+    pinned float prompt pass (bit for bit in float64), with ragged prompts,
+    cached prefixes and an empty prompt."""
+    nb, h, hq, d = 40, 2, 8, 16
+    kc, vc, ks, vs = _int8_pools(60, nb, h, d, pow2_scales=True)
+    qlens = [5, 0, 33, 17]
+    ctx = [5, 9, 70, 40]
+    bt = _tables(61, nb, ctx)
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int64)
+    q = torch.randn((int(cu[-1]), hq, d), generator=torch.Generator().manual_seed(62)).numpy()
+    kf = ks[..., None].astype(np.float64) * kc.astype(np.float64)
+    vf = vs[..., None].astype(np.float64) * vc.astype(np.float64)
+    want = oracle.prefill_ref(q, kf, vf, bt, cu, np.array(ctx), 0.3)
+    got = oracle.prefill_int8_ref(q, kc, vc, ks, vs, bt, cu, np.array(ctx), 0.3)
+    assert np.array_equal(got, want)
+    # a subset of rows leaves the others zero and computes the same values
+    sub = oracle.prefill_int8_ref(q, kc, vc, ks, vs, bt, cu, np.array(ctx), 0.3, rows=[0, 40])
+    assert np.array_equal(sub[[0, 40]], want[[0, 40]]) and not sub[1:40].any()
+
+
+def test_prefill_int8_is_the_verification_of_the_whole_prompt():
+    """A sequence whose q_len rows are its last q_len positions: the prompt pass
+    over those rows is the INT8 verification pass with that q_len (float64,
+    to rounding order), on arbitrary codes and scales."""
+    nb, h, hq, d = 20, 2, 4, 8
+    kc, vc, ks, vs = _int8_pools(63, nb, h, d)
+    ctx, ql = [37, 12], 12
+    bt = _tables(64, nb, ctx)
+    q = torch.randn((len(ctx), ql, hq, d), generator=torch.Generator().manual_seed(65)).numpy()
+    want = oracle.verify_int8_ref(q, kc, vc, ks, vs, bt, np.array(ctx), 0.4)
+    cu = np.arange(len(ctx) + 1, dtype=np.int64) * ql
+    got = oracle.prefill_int8_ref(q.reshape(-1, hq, d), kc, vc, ks, vs, bt, cu, np.array(ctx), 0.4)
+    assert np.max(np.abs(got.reshape(want.shape) - want)) < 1e-12
 
 
 def test_verify_int8_first_query_of_a_fresh_context_sees_one_key():
