@@ -619,7 +619,7 @@ def run_ours(args, rank, world, local_rank):
 N_LAYERS = {"tiny_fp32": 1, "llama32_1b_decode": 16, "llama3_8b_decode": 32, "prefix_shared_8k": 32,
             "mixed_mistral7b": 32, "llama3_8b_long_b1": 32, "llama3_8b_long_b4": 32,
             "llama32_1b_decode_int8": 16, "llama3_8b_decode_int8": 32, "llama3_8b_verify": 32,
-            "llama3_8b_verify_int8": 32, "llama3_8b_decode_rope": 32}
+            "llama3_8b_verify_int8": 32, "llama3_8b_decode_rope": 32, "mixed_mistral7b_int8": 32}
 # The five configurations of the benchmark's workload list, then the small-batch
 # end of its decode range (batch 1 and 4 at contexts up to 8192).
 CONFIGS = ["tiny_fp32", "llama32_1b_decode", "llama3_8b_decode", "prefix_shared_8k", "mixed_mistral7b",
@@ -682,6 +682,11 @@ def measure_workload(name, pa, W, torch, dev, reps, warmup, partition=0, flush=N
         for d in d_in:
             d["pos"] = (d["ctx"] - 1).to(torch.int32)
             d["q0"] = d["q"].clone()
+    pws = None
+    if wl.prompt_lens and wl.kv_int8:   # the INT8 prompt pass dequantises into its workspace
+        mp = max(wl.prompt_lens)
+        pws = torch.empty(max(1, pa.pa_prefill_int8_workspace_size(len(wl.prompt_lens), hq, mp, mp, kp, wl.dtype)),
+                          dtype=torch.uint8, device=dev)
     flush = flush or l2_flusher(torch, dev)
     stream = torch.cuda.current_stream()
     rec = {"append": [], "prefill": [], "decode": []}
@@ -702,7 +707,11 @@ def measure_workload(name, pa, W, torch, dev, reps, warmup, partition=0, flush=N
         else:
             pa.pa_append_kv(kp, vp, d["slots"], d["kn"], d["vn"], stream=stream)
         evs[1].record(stream)
-        if wl.prompt_lens:
+        if wl.prompt_lens and wl.kv_int8:
+            pa.pa_prefill_attention_int8(d["pout"], d["qp"], kp, vp, ks, vs, pbt, d["cu"], d["pctx"], wl.scale,
+                                         max_q_len=max(wl.prompt_lens), max_context_len=max(wl.prompt_lens),
+                                         workspace=pws, stream=stream)
+        elif wl.prompt_lens:
             pa.pa_prefill_attention(d["pout"], d["qp"], kp, vp, pbt, d["cu"], d["pctx"], wl.scale,
                                     max_q_len=max(wl.prompt_lens), max_context_len=max(wl.prompt_lens),
                                     stream=stream)

@@ -70,7 +70,8 @@ enum {
   PA_DEV_BAD_BLOCK_ID = 2,    /* a block-table entry outside [0, num_blocks) (skipped) */
   PA_DEV_BAD_CONTEXT = 4,     /* context_len < 0 or > max_blocks_per_seq*16 (clamped) */
   PA_DEV_WAIT_TIMEOUT = 8,    /* a bounded wait on a copy barrier gave up              */
-  PA_DEV_BAD_POSITION = 16    /* RoPE: position outside [0, max_positions) (row skipped) */
+  PA_DEV_BAD_POSITION = 16,   /* RoPE: position outside [0, max_positions) (row skipped) */
+  PA_DEV_RANGE = 32           /* INT8 prompt pass: a value past fp16's range (clamped) */
 };
 
 /* Geometry of the KV pool, shared by every call. */
@@ -350,6 +351,39 @@ PA_API int pa_verify_attention_int8(void* out, const void* q, const void* k_code
                                     int max_context_len, int partition_size, int act_dtype,
                                     const pa_pool_desc* pool, void* workspace,
                                     size_t workspace_bytes, void* stream);
+
+/*
+ * pa_prefill_attention_int8 -- pa_prefill_attention over an INT8 cache: the
+ * causal prompt pass (all prompt tokens at once, "LLM Inference Server",
+ * Stage 1) with keys and values x_hat = scales[row] * codes[row][d].  The
+ * pass is compute-bound, so each sequence's blocks of its first
+ * context_lens[s] positions are first dequantised into `workspace` (every
+ * x_hat rounded once to fp16, 11 significant bits, in the float pool layout),
+ * and the fp16 prompt pass runs over those copies; bf16 queries are converted
+ * to fp16 (exactly, within fp16's range) and the output back to bf16.
+ *   out, q   : act_dtype [cu_q_lens[num_seqs]][num_q_heads][D]
+ *   the other arguments as pa_prefill_attention; pool->dtype = PA_I8
+ *   workspace: device, 16-byte aligned, >= pa_prefill_int8_workspace_size()
+ *              bytes, owned by the caller, its contents scratch: the fp16 K
+ *              and V copies of num_seqs x ceil(max_context_len / 16) blocks
+ *              and their block table, and for bf16 activations fp16 copies of
+ *              num_seqs x max_q_len rows of q and of out.
+ * Errors as pa_prefill_attention, plus PA_ERR_INVALID for a missing or small
+ * workspace and PA_ERR_UNSUPPORTED past 65535 sequences.  A block id outside
+ * the pool sets PA_DEV_BAD_BLOCK_ID and its keys read as zeros; a cache or
+ * query value past fp16's range (|x| > 65504) is clamped and sets PA_DEV_RANGE.
+ */
+PA_API size_t pa_prefill_int8_workspace_size(int num_seqs, int num_q_heads, int max_q_len,
+                                             int max_context_len, int act_dtype,
+                                             const pa_pool_desc* pool);
+PA_API int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes,
+                                     const void* v_codes, const float* k_scales,
+                                     const float* v_scales, const int32_t* block_tables,
+                                     const int32_t* cu_q_lens, const int32_t* context_lens,
+                                     float scale, int num_seqs, int num_q_heads,
+                                     int max_blocks_per_seq, int max_q_len, int max_context_len,
+                                     int act_dtype, const pa_pool_desc* pool, void* workspace,
+                                     size_t workspace_bytes, void* stream);
 
 /*
  * Rotary position embedding fused into the append.  The pages name RoPE as a

@@ -21,6 +21,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = 0, -1, -
 PA_ERR_NO_BLOCKS = -5
 PA_DEV_BAD_SLOT, PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_CONTEXT, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 PA_DEV_BAD_POSITION = 16
+PA_DEV_RANGE = 32
 BLOCK_SIZE = 16
 
 _DTYPES = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16, torch.int8: PA_I8}
@@ -120,6 +121,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_verify_attention_int8.restype = i32
     L.pa_verify_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
                                            i32, pdesc, vp, sz, vp]
+    L.pa_prefill_int8_workspace_size.restype = sz
+    L.pa_prefill_int8_workspace_size.argtypes = [i32, i32, i32, i32, i32, pdesc]
+    L.pa_prefill_attention_int8.restype = i32
+    L.pa_prefill_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
+                                            pdesc, vp, sz, vp]
     _lib = L
     return L
 
@@ -480,6 +486,50 @@ def pa_verify_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.
                                       hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
                                       _act(q), ctypes.byref(desc), _ptr(workspace), int(ws_bytes),
                                       _stream(stream)))
+
+def pa_prefill_int8_workspace_size(num_seqs: int, num_q_heads: int, max_q_len: int, max_context_len: int,
+                                   k_codes: torch.Tensor, act_dtype: torch.dtype) -> int:
+    """Bytes of workspace pa_prefill_attention_int8 needs (k_codes: the int8
+    pool; act_dtype: torch.bfloat16 or torch.float16)."""
+    L = load_library()
+    desc = pool_desc(k_codes)
+    n = L.pa_prefill_int8_workspace_size(int(num_seqs), int(num_q_heads), int(max_q_len), int(max_context_len),
+                                         _DTYPES[act_dtype], ctypes.byref(desc))
+    msg = pa_last_error()
+    if msg:
+        raise PaError(PA_ERR_INVALID, msg)
+    return int(n)
+
+
+def pa_prefill_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                              k_scales: torch.Tensor, v_scales: torch.Tensor, block_tables: torch.Tensor,
+                              cu_q_lens: torch.Tensor, context_lens: torch.Tensor, scale: float, max_q_len: int,
+                              max_context_len: int, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pa_prefill_attention over an INT8 cache; out, q: [sum q_len][H_q][D]
+    bf16/fp16.  ``workspace``: a device uint8 tensor of at least
+    pa_prefill_int8_workspace_size() bytes (allocated here when omitted)."""
+    desc = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables), ("cu_q_lens", cu_q_lens),
+                 ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _need(q.dim() == 3 and q.shape[2] == k_codes.shape[3], "q must be [sum q_len][H_q][D]")
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out/q shape or dtype mismatch")
+    S = int(context_lens.shape[0])
+    _need(cu_q_lens.dtype == torch.int32 and tuple(cu_q_lens.shape) == (S + 1,), "cu_q_lens must be int32 [S+1]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == S,
+          "block_tables must be int32 [S][max_blocks]")
+    L = load_library()
+    if workspace is None:
+        need = pa_prefill_int8_workspace_size(S, int(q.shape[1]), max_q_len, max_context_len, k_codes, q.dtype)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.pa_prefill_attention_int8(_ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales),
+                                       _ptr(v_scales), _ptr(block_tables), _ptr(cu_q_lens), _ptr(context_lens),
+                                       float(scale), S, int(q.shape[1]), int(block_tables.shape[1]), int(max_q_len),
+                                       int(max_context_len), _act(q), ctypes.byref(desc), _ptr(workspace),
+                                       int(ws_bytes), _stream(stream)))
+
 
 # ---------------------------------------------------------------------------
 # rotary position embedding (half-split, Llama form)

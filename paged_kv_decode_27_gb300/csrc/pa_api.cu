@@ -595,30 +595,13 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
   return PA_OK;
 }
 
-int pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
-                         const int32_t* block_tables, const int32_t* cu_q_lens, const int32_t* context_lens,
-                         float scale, int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_q_len,
-                         int max_context_len, const pa_pool_desc* pool, void* stream) {
-  t_err.clear();
-  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, 0, pool);
-  if (rc != PA_OK) return rc;
-  if ((rc = reject_int8(pool)) != PA_OK) return rc;
-  if (pool->dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "prefill needs bf16 or fp16 pools");
-  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
-  if (max_q_len < 0 || max_q_len > max_context_len)
-    return fail(PA_ERR_INVALID, "max_q_len %d must be in [0, max_context_len=%d]", max_q_len, max_context_len);
-  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
-  if (!out || !q || !k_pool || !v_pool || !block_tables || !cu_q_lens || !context_lens)
-    return fail(PA_ERR_INVALID, "null pointer argument");
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
-    return fail(PA_ERR_INVALID, "out, q and the pools must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
-    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
-  if ((max_q_len + 63) / 64 > 0x7fffffff) return fail(PA_ERR_UNSUPPORTED, "max_q_len too large");
-  int* status = status_ptr();
-  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+namespace {
 
+// The prompt pass over a bf16/fp16 pool once the call has been validated.
+int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                   const int32_t* cu_q_lens, const int32_t* context_lens, float scale, int num_seqs,
+                   int num_q_heads, int max_blocks_per_seq, int max_q_len, const pa_pool_desc* pool, int* status,
+                   void* stream) {
   pa::PrefillArgs a{};
   a.out = out;
   a.q = q;
@@ -635,6 +618,7 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   a.max_q_len = max_q_len;
   a.status = status;
   CUtensorMap kmap, vmap, qmap;
+  int rc;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
   if ((rc = make_q_map(&qmap, q, pool->dtype, num_q_heads, pool->head_dim,
@@ -642,6 +626,146 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
     return rc;
   cudaError_t e = pa::launch_prefill_umma(a, pool->dtype, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return PA_OK;
+}
+
+// Checks shared by the prompt passes (pool already checked): returns PA_OK, or
+// the error of the first violated rule.  Sets *nothing when there is no work.
+int check_prefill_args(const void* out, const void* q, const int32_t* block_tables, const int32_t* cu_q_lens,
+                       const int32_t* context_lens, float scale, int num_seqs, int max_q_len, int max_context_len,
+                       bool* nothing) {
+  *nothing = false;
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
+  if (max_q_len < 0 || max_q_len > max_context_len)
+    return fail(PA_ERR_INVALID, "max_q_len %d must be in [0, max_context_len=%d]", max_q_len, max_context_len);
+  if (num_seqs == 0 || max_q_len == 0) {
+    *nothing = true;
+    return PA_OK;
+  }
+  if (!out || !q || !block_tables || !cu_q_lens || !context_lens) return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q)) return fail(PA_ERR_INVALID, "out and q must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
+  if ((max_q_len + 63) / 64 > 0x7fffffff) return fail(PA_ERR_UNSUPPORTED, "max_q_len too large");
+  return PA_OK;
+}
+
+// Workspace of the INT8 prompt pass: the fp16 copies of the K and V blocks
+// (num_seqs * B blocks, B = blocks of max_context_len), their block table, and
+// for bf16 activations fp16 copies of q and of the output (num_seqs *
+// max_q_len rows at most).
+struct PrefillQ8Ws {
+  size_t k_off, v_off, table_off, q_off, out_off, total;
+  int B;
+};
+
+PrefillQ8Ws prefill_q8_ws(int num_seqs, int num_q_heads, int max_q_len, int max_context_len, int act_dtype,
+                          const pa_pool_desc* pool) {
+  PrefillQ8Ws w{0, 0, 0, 0, 0, 0, 0};
+  w.B = (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  const size_t blocks = static_cast<size_t>(num_seqs) * w.B;
+  if (blocks == 0 || max_q_len == 0) return w;
+  const size_t pool_bytes = blocks * pool->num_kv_heads * PA_BLOCK_SIZE * pool->head_dim * 2;
+  const size_t rows_bytes = static_cast<size_t>(num_seqs) * max_q_len * num_q_heads * pool->head_dim * 2;
+  w.k_off = 0;
+  w.v_off = align256(pool_bytes);
+  w.table_off = w.v_off + align256(pool_bytes);
+  w.q_off = w.table_off + align256(blocks * sizeof(int32_t));
+  w.out_off = w.q_off + (act_dtype == PA_BF16 ? align256(rows_bytes) : 0);
+  w.total = w.out_off + (act_dtype == PA_BF16 ? rows_bytes : 0);
+  if (act_dtype != PA_BF16) w.total = w.table_off + blocks * sizeof(int32_t);
+  return w;
+}
+
+}  // namespace
+
+int pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, const int32_t* cu_q_lens, const int32_t* context_lens,
+                         float scale, int num_seqs, int num_q_heads, int max_blocks_per_seq, int max_q_len,
+                         int max_context_len, const pa_pool_desc* pool, void* stream) {
+  t_err.clear();
+  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, 0, pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = reject_int8(pool)) != PA_OK) return rc;
+  if (pool->dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "prefill needs bf16 or fp16 pools");
+  bool nothing;
+  if ((rc = check_prefill_args(out, q, block_tables, cu_q_lens, context_lens, scale, num_seqs, max_q_len,
+                               max_context_len, &nothing)) != PA_OK)
+    return rc;
+  if (nothing) return PA_OK;
+  if (!k_pool || !v_pool) return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return fail(PA_ERR_INVALID, "the pools must be 16-byte aligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  return prefill_launch(out, q, k_pool, v_pool, block_tables, cu_q_lens, context_lens, scale, num_seqs, num_q_heads,
+                        max_blocks_per_seq, max_q_len, pool, status, stream);
+}
+
+size_t pa_prefill_int8_workspace_size(int num_seqs, int num_q_heads, int max_q_len, int max_context_len,
+                                      int act_dtype, const pa_pool_desc* pool) {
+  t_err.clear();
+  if (check_pool(pool) != PA_OK) return 0;
+  if (check_int8(pool, act_dtype) != PA_OK) return 0;
+  if (num_seqs < 0 || num_q_heads < 1 || max_q_len < 0 || max_context_len < 0) {
+    fail(PA_ERR_INVALID, "num_seqs, max_q_len and max_context_len must be >= 0, num_q_heads >= 1");
+    return 0;
+  }
+  return prefill_q8_ws(num_seqs, num_q_heads, max_q_len, max_context_len, act_dtype, pool).total;
+}
+
+int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                              const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                              const int32_t* cu_q_lens, const int32_t* context_lens, float scale, int num_seqs,
+                              int num_q_heads, int max_blocks_per_seq, int max_q_len, int max_context_len,
+                              int act_dtype, const pa_pool_desc* pool, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  t_err.clear();
+  int rc = check_decode_shape(num_seqs, num_q_heads, max_blocks_per_seq, max_context_len, 0, pool);
+  if (rc != PA_OK) return rc;
+  if ((rc = check_int8(pool, act_dtype)) != PA_OK) return rc;
+  bool nothing;
+  if ((rc = check_prefill_args(out, q, block_tables, cu_q_lens, context_lens, scale, num_seqs, max_q_len,
+                               max_context_len, &nothing)) != PA_OK)
+    return rc;
+  if (nothing) return PA_OK;
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences in one INT8 prompt pass");
+  if (static_cast<long long>(num_seqs) * ((max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE) > 0x7fffffffLL)
+    return fail(PA_ERR_UNSUPPORTED, "num_seqs x context blocks too large");
+  if (!k_codes || !v_codes || !k_scales || !v_scales) return fail(PA_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
+    return fail(PA_ERR_INVALID, "codes and scales must be 16-byte aligned");
+  const PrefillQ8Ws ws = prefill_q8_ws(num_seqs, num_q_heads, max_q_len, max_context_len, act_dtype, pool);
+  if (!workspace) return fail(PA_ERR_INVALID, "workspace of %zu bytes required, got NULL", ws.total);
+  if (workspace_bytes < ws.total)
+    return fail(PA_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, ws.total);
+  if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+  int* status = status_ptr();
+  if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  int32_t* table = reinterpret_cast<int32_t*>(base + ws.table_off);
+  cudaError_t e = pa::launch_dequant_q8(k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, num_seqs,
+                                        max_blocks_per_seq, pool->num_kv_heads, pool->head_dim, pool->num_blocks,
+                                        ws.B, base + ws.k_off, base + ws.v_off, table, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "INT8 prompt-pass dequantisation launch");
+  // the pass runs in fp16: bf16 queries in, fp16 output back to bf16
+  const bool bf = act_dtype == PA_BF16;
+  const int width = num_q_heads * pool->head_dim;
+  const void* q16 = q;
+  void* out16 = out;
+  if (bf) {
+    q16 = base + ws.q_off;
+    out16 = base + ws.out_off;
+    if ((e = pa::launch_convert_rows(q, base + ws.q_off, cu_q_lens, num_seqs, width, true, status, st)) != cudaSuccess)
+      return cuda_fail(e, "INT8 prompt-pass query conversion launch");
+  }
+  const pa_pool_desc fpool{num_seqs * ws.B, pool->num_kv_heads, pool->block_size, pool->head_dim, PA_F16};
+  rc = prefill_launch(out16, q16, base + ws.k_off, base + ws.v_off, table, cu_q_lens, context_lens, scale, num_seqs,
+                      num_q_heads, ws.B, max_q_len, &fpool, status, stream);
+  if (rc != PA_OK || !bf) return rc;
+  if ((e = pa::launch_convert_rows(out16, out, cu_q_lens, num_seqs, width, false, status, st)) != cudaSuccess)
+    return cuda_fail(e, "INT8 prompt-pass output conversion launch");
   return PA_OK;
 }
 

@@ -368,10 +368,11 @@ def prefix_shared_8k() -> Workload:
                     extra={"shared_prefix_blocks": shared, "blocks_used": used})
 
 
-def mixed_mistral7b() -> Workload:
+def mixed_mistral7b(kv: str = "float") -> Workload:
     """One continuous-batching step, Mistral-7B-shaped (h_q=32, h_kv=8, D=128,
     bf16): 4 causal prompts of 512/1024/1536/2048 tokens written into the pool
-    and 60 decode sequences with contexts uniform in [256, 4096]."""
+    and 60 decode sequences with contexts uniform in [256, 4096].
+    ``kv="int8"``: the same step over an INT8 cache."""
     cid = 5
     g = torch.Generator().manual_seed(1000 + cid)
     prompts = [512, 1024, 1536, 2048]
@@ -379,14 +380,15 @@ def mixed_mistral7b() -> Workload:
     need = [_blocks_for(L) for L in prompts] + [_blocks_for(int(c)) for c in ctx0]
     pool_blocks = int(math.ceil(1.25 * sum(need)))
     bt = _assign_blocks(need, pool_blocks, g)
-    k_pool = _pool(pool_blocks, 8, 128, torch.bfloat16, 1.0, g)
-    v_pool = _pool(pool_blocks, 8, 128, torch.bfloat16, 1.0, g)
-    return Workload(name="mixed_mistral7b", config_id=cid, dtype=torch.bfloat16,
-                    num_q_heads=32, num_kv_heads=8, head_dim=128, scale=1.0 / math.sqrt(128),
+    k_pool, v_pool, k_scales, v_scales = _kv_pools(pool_blocks, 8, 128, torch.bfloat16, 1.0, g, kv)
+    return Workload(name="mixed_mistral7b" + ("_int8" if kv == "int8" else ""), config_id=cid,
+                    dtype=torch.bfloat16, num_q_heads=32, num_kv_heads=8, head_dim=128, scale=1.0 / math.sqrt(128),
                     steps=1, k_pool=k_pool, v_pool=v_pool, block_tables=bt,
                     ctx0=ctx0.to(torch.int32), decode_rows=slice(4, 64),
                     prefill_rows=slice(0, 4), prompt_lens=prompts,
-                    description="mixed continuous-batching step (Mistral-7B-shaped), bf16")
+                    k_scales=k_scales, v_scales=v_scales,
+                    description="mixed continuous-batching step (Mistral-7B-shaped), bf16" +
+                                (", INT8 KV cache" if kv == "int8" else ""))
 
 
 WORKLOADS = {
@@ -395,6 +397,7 @@ WORKLOADS = {
     "llama3_8b_decode": llama3_8b_decode,
     "prefix_shared_8k": prefix_shared_8k,
     "mixed_mistral7b": mixed_mistral7b,
+    "mixed_mistral7b_int8": lambda: mixed_mistral7b(kv="int8"),
     "llama32_1b_decode_int8": lambda: llama32_1b_decode(kv="int8"),
     "llama3_8b_decode_int8": lambda: llama3_8b_decode(kv="int8"),
     "llama3_8b_verify": lambda: llama3_8b_verify(),

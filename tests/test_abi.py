@@ -105,6 +105,37 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert call(_desc(), out=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
 
 
+def test_int8_prefill_validates_on_the_host(lib):
+    """The INT8 prompt pass: the pool must be INT8 with a bf16/fp16 act_dtype,
+    the workspace present and large enough.  The workspace is the fp16 K and V
+    copies of num_seqs x ceil(max_context_len / 16) blocks and their int32
+    block table (each part 256-byte aligned), and for bf16 activations fp16
+    copies of num_seqs x max_q_len rows of q and of the output."""
+    f = ctypes.c_void_p(FAKE)
+    i8 = _desc(dt=B.PA_I8)
+    al = lambda n: ((n + 255) // 256) * 256
+    pool = 2 * 4 * 8 * 16 * 128 * 2                      # 2 seqs x 4 blocks x 8 heads x 16 x 128 x 2 bytes
+    rows = 2 * 64 * 32 * 128 * 2                         # 2 seqs x 64 rows x 32 heads x 128 x 2 bytes
+    f16 = lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_F16, ctypes.byref(i8))
+    assert f16 == 2 * al(pool) + 2 * 4 * 4
+    size = lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_BF16, ctypes.byref(i8))
+    assert size == 2 * al(pool) + al(2 * 4 * 4) + al(rows) + rows
+    assert lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_BF16, ctypes.byref(_desc(dt=B.PA_BF16))) == 0
+    assert lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_F32, ctypes.byref(i8)) == 0
+    call = lambda desc, act=B.PA_BF16, ws=f, wsb=size, maxq=64, maxc=64, S=2: lib.pa_prefill_attention_int8(
+        f, f, f, f, f, f, f, f, f, 0.1, S, 32, 4, maxq, maxc, act, ctypes.byref(desc), ws, wsb, None)
+    assert call(_desc(dt=B.PA_BF16)) == B.PA_ERR_INVALID          # float pool
+    assert call(i8, act=B.PA_F32) == B.PA_ERR_INVALID
+    assert call(i8, ws=ctypes.c_void_p(0)) == B.PA_ERR_INVALID    # no workspace
+    assert call(i8, wsb=size - 1) == B.PA_ERR_INVALID              # too small
+    assert call(i8, act=B.PA_F16, wsb=f16 - 1) == B.PA_ERR_INVALID
+    assert call(i8, maxq=65) == B.PA_ERR_INVALID
+    assert call(i8, S=0) == B.PA_OK                                # nothing to do
+    # the float prompt pass refuses the INT8 pool
+    assert lib.pa_prefill_attention(f, f, f, f, f, f, f, 0.1, 2, 32, 4, 64, 64, ctypes.byref(i8), None) == \
+        B.PA_ERR_INVALID
+
+
 def test_workspace_size_and_partition(lib):
     d = _desc(d=128)
     # batch 64, 8 KV heads, contexts to 8224: 1024-token partitions, 9 splits

@@ -13,6 +13,7 @@ import torch
 import oracle
 from paged_kv_decode_27_gb300 import binding as pa
 from paged_kv_decode_27_gb300 import workloads as W
+from _gpu import oracle_append
 from _util import assert_close_to_ref, to_np
 
 pytestmark = pytest.mark.gpu
@@ -371,4 +372,128 @@ def test_verify_int8_llama3_8b_full_size():
     out = _verify8(wl, cache, q, st.context_lens, max_ctx=wl.max_context_len(0))
     ref = _verify8_ref(wl, cache, q, st.context_lens)
     assert_close_to_ref(out, ref, wl.dtype, "int8 verify llama3-8b")
+    assert pa.pa_device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# prompt pass (causal over each prompt and its cached prefix) over the cache
+# ---------------------------------------------------------------------------
+
+def _nan_unused_scales(wl, ctx):
+    """Every scale slot that no sequence's context covers becomes NaN, so a
+    read past a context (or of a block outside it) shows up in the output."""
+    used = set()
+    for s in range(wl.block_tables.shape[0]):
+        for p in range(int(ctx[s])):
+            used.add((int(wl.block_tables[s, p // 16]), p % 16))
+    for sc in (wl.k_scales, wl.v_scales):
+        for b in range(sc.shape[0]):
+            for o in range(16):
+                if (b, o) not in used:
+                    sc[b, :, o] = float("nan")
+
+
+def _prefill8(wl, cache, q, cu, ctx, bt=None):
+    out = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    qlens = cu[1:] - cu[:-1]
+    bt = wl.block_tables if bt is None else bt
+    pa.pa_prefill_attention_int8(out, q.to(DEV), cache.kc, cache.vc, cache.ks, cache.vs, bt.contiguous().to(DEV),
+                                 cu.to(DEV), ctx.to(DEV), wl.scale, max_q_len=int(qlens.max()),
+                                 max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    return out
+
+
+def _prefill8_case(seed, qlens, prior, hq, hkv, d, dtype):
+    ctx = [a + b for a, b in zip(qlens, prior)]
+    wl = W.small_random(seed, len(ctx), 0, hq, hkv, d, dtype, ctx=ctx, kv="int8")
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn((sum(qlens), hq, d), generator=g).to(dtype)
+    cu = torch.tensor([0] + list(np.cumsum(qlens)), dtype=torch.int32)
+    return wl, q, cu, torch.tensor(ctx, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("qlens,prior", [
+    ([1, 15, 16, 17, 63, 64, 65, 130], [0] * 8),
+    ([5, 64, 100], [40, 3, 200]),          # cached prefix before the prompt
+    ([257], [0]),
+])
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(32, 8, 128, torch.bfloat16), (8, 8, 64, torch.bfloat16),
+                                            (16, 2, 64, torch.float16), (12, 4, 128, torch.float16)])
+def test_prefill_int8_small(qlens, prior, hq, hkv, d, dtype):
+    """Ragged prompts, cached prefixes, every 16-token block edge; the scales
+    of every slot outside the contexts are NaN."""
+    wl, q, cu, ctx = _prefill8_case(140 + sum(qlens) + d + hq, qlens, prior, hq, hkv, d, dtype)
+    _nan_unused_scales(wl, ctx)
+    cache = Cache(wl)
+    out = _prefill8(wl, cache, q, cu, ctx)
+    ref = oracle.prefill_int8_ref(to_np(q), *cache.host, wl.block_tables.numpy(), cu.numpy(), ctx.numpy(),
+                                  wl.scale)
+    assert_close_to_ref(out, ref, dtype, f"int8 prefill G={hq // hkv} d={d}")
+    assert pa.pa_device_status() == 0
+
+
+def test_prefill_int8_bad_block_id_is_reported():
+    wl, q, cu, ctx = _prefill8_case(150, [40, 70, 33], [0, 30, 0], 32, 8, 128, torch.bfloat16)
+    cache = Cache(wl)
+    out = _prefill8(wl, cache, q, cu, ctx)
+    assert pa.pa_device_status() == 0
+    bt = wl.block_tables.clone()
+    bt[1, 2] = wl.k_pool.shape[0] + 5
+    out2 = _prefill8(wl, cache, q, cu, ctx, bt)
+    assert pa.pa_device_status() & pa.PA_DEV_BAD_BLOCK_ID
+    assert torch.equal(out2[:40], out[:40]) and torch.equal(out2[110:], out[110:])   # sequences 0 and 2
+
+
+def test_prefill_int8_matches_the_float_pass_on_its_dequantised_pools():
+    """Consistency check, not parity evidence: on a cache whose x_hat is exactly
+    representable in fp16 (power-of-two scales, 8-bit codes), the INT8 prompt
+    pass with fp16 activations and the fp16 prompt pass over the same values
+    agree bit for bit."""
+    wl, q, cu, ctx = _prefill8_case(151, [100, 37], [20, 60], 32, 8, 128, torch.float16)
+    g = torch.Generator().manual_seed(152)
+    e = torch.randint(-8, -2, wl.k_scales.shape, generator=g).to(torch.float32)
+    wl.k_scales.copy_(torch.exp2(e))
+    wl.v_scales.copy_(torch.exp2(e.flip(0)))
+    cache = Cache(wl)
+    out8 = _prefill8(wl, cache, q, cu, ctx)
+    kf = (wl.k_scales[..., None].double() * wl.k_pool.double()).to(torch.float16).to(DEV)
+    vf = (wl.v_scales[..., None].double() * wl.v_pool.double()).to(torch.float16).to(DEV)
+    outf = torch.empty_like(out8)
+    pa.pa_prefill_attention(outf, q.to(DEV), kf, vf, wl.block_tables.contiguous().to(DEV), cu.to(DEV),
+                            ctx.to(DEV), wl.scale, max_q_len=100, max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    assert torch.equal(out8, outf)
+
+
+def test_prefill_int8_mixed_mistral7b_prompts():
+    """The four prompts (512..2048 tokens) of the mixed Mistral-7B-shaped step
+    over an INT8 cache (the prompts' K and V quantised by the oracle's rule),
+    every query row against the oracle."""
+    wl = W.mixed_mistral7b()
+    st = wl.step(0)
+    k_np, v_np = oracle_append(wl, st)
+    ctx = st.prefill_context_lens
+    bt = wl.prefill_block_tables
+    kc = np.zeros(k_np.shape, dtype=np.int8)
+    vc = np.zeros(v_np.shape, dtype=np.int8)
+    ks = np.zeros(k_np.shape[:3], dtype=np.float32)
+    vs = np.zeros(v_np.shape[:3], dtype=np.float32)
+    for s in range(len(ctx)):
+        for b in range((int(ctx[s]) + 15) // 16):
+            blk = int(bt[s, b])
+            kc[blk], ks[blk] = oracle.quantize_rows_int8(k_np[blk])
+            vc[blk], vs[blk] = oracle.quantize_rows_int8(v_np[blk])
+    cache = type("C", (), {})()
+    cache.kc, cache.vc = torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV)
+    cache.ks, cache.vs = torch.from_numpy(ks).to(DEV), torch.from_numpy(vs).to(DEV)
+    q = st.q_prefill
+    out = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    pa.pa_prefill_attention_int8(out, q.to(DEV), cache.kc, cache.vc, cache.ks, cache.vs, bt.contiguous().to(DEV),
+                                 st.cu_q_lens.to(DEV), ctx.to(DEV), wl.scale,
+                                 max_q_len=int((st.cu_q_lens[1:] - st.cu_q_lens[:-1]).max()),
+                                 max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    ref = oracle.prefill_int8_ref(to_np(q), kc, vc, ks, vs, bt.numpy(), st.cu_q_lens.numpy(), ctx.numpy(), wl.scale)
+    assert_close_to_ref(out, ref, wl.dtype, "int8 mixed prefill")
     assert pa.pa_device_status() == 0
