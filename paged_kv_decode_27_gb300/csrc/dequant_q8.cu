@@ -19,11 +19,15 @@
 // outside the pool is reported and its copy holds zeros.
 //
 // bf16 queries are converted to fp16 for the pass (exact for |q| in fp16's
-// normal range: bf16 carries 8 significant bits) and its fp16 output back to
-// bf16.
+// normal range: bf16 carries 8 significant bits); the pass stores its output
+// rows as bf16 itself.
 //
-// One CTA per (sequence, block); a thread widens 16 codes of a row (one
-// 16-byte load, two 16-byte stores) for K and then V.
+// One launch does both: a CTA per (sequence, block), where a thread widens 16
+// codes of a row (one 16-byte load, two 16-byte stores), eight such chunks
+// with their loads issued together, and 4 x SMs CTAs streaming the query
+// conversion.  The dequantisation waits on load latency (context length and
+// block id, then the codes), the conversion on bandwidth, so each runs in the
+// other's idle time.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -59,104 +63,120 @@ __device__ __forceinline__ void widen16(const uint4 w, float s, uint4& lo, uint4
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-__global__ void __launch_bounds__(256)
-dequant_blocks_q8_kernel(const int8_t* __restrict__ k_codes, const int8_t* __restrict__ v_codes,
-                         const float* __restrict__ k_scales, const float* __restrict__ v_scales,
-                         const int32_t* __restrict__ block_tables, const int32_t* __restrict__ context_lens,
-                         int max_blocks_per_seq, int num_kv_heads, int head_dim, int num_blocks, int B,
-                         __half* __restrict__ k_out, __half* __restrict__ v_out, int32_t* __restrict__ table_out,
-                         int* status) {
-  grid_dependency_wait();   // the prompt's rows were appended by the kernel before us
-  const int lb = blockIdx.x;
-  const int s = blockIdx.y;
-  const size_t ob = static_cast<size_t>(s) * B + lb;   // block of the copies
-  if (threadIdx.x == 0) table_out[ob] = static_cast<int32_t>(ob);
-  const int c = __ldg(context_lens + s);
-  if (lb * kBlock >= c) return;
-  const int id = __ldg(block_tables + static_cast<size_t>(s) * max_blocks_per_seq + lb);
-  const bool live = id >= 0 && id < num_blocks;
-  if (!live && threadIdx.x == 0) flag_status(status, PA_DEV_BAD_BLOCK_ID);
-  const int chunks = head_dim / 16;                     // 16-code chunks per row
-  const int per_block = num_kv_heads * kBlock * chunks; // chunks per (block, K or V)
-  const size_t src0 = static_cast<size_t>(live ? id : 0) * num_kv_heads * kBlock;   // first row of the block
-  const size_t dst0 = ob * num_kv_heads * kBlock;
-  bool out_of_range = false;
-  for (int i = threadIdx.x; i < 2 * per_block; i += blockDim.x) {
-    const bool is_k = i < per_block;
-    const int j = is_k ? i : i - per_block;
-    const int row = j / chunks;                          // (head, slot) row within the block
-    const int ch = j - row * chunks;
-    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-    // rows past the context (stale slots of the last block) are written as zeros
-    if (live && lb * kBlock + row % kBlock < c) {
-      const int8_t* codes = is_k ? k_codes : v_codes;
-      const float* scales = is_k ? k_scales : v_scales;
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(codes + (src0 + row) * head_dim) + ch);
-      widen16(w, __ldg(scales + src0 + row), lo, hi, out_of_range);
-    }
-    uint4* dst = reinterpret_cast<uint4*>((is_k ? k_out : v_out) + (dst0 + row) * head_dim) + 2 * ch;
-    dst[0] = lo;
-    dst[1] = hi;
-  }
-  if (out_of_range) flag_status(status, PA_DEV_RANGE);
-}
+// One CTA dequantises one (sequence, block): every load of a thread's chunks
+// (kUnrollBlock of them) is issued before the first is used, and the context
+// length and block id are read together, so a CTA waits on two load latencies.
+constexpr int kUnrollBlock = 8;
+constexpr int kUnrollRows = 4;
 
-// Rows 0 .. cu_q_lens[num_seqs] - 1 of [rows][width] (width a multiple of 8)
-// converted between bf16 and fp16: TO_HALF bf16 -> fp16 (clamped to fp16's
-// range, reported), else fp16 -> bf16.
-template <bool TO_HALF>
-__global__ void __launch_bounds__(256)
-convert_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, const int32_t* __restrict__ cu_q_lens,
-                    int num_seqs, int width, int* status) {
-  grid_dependency_wait();
-  const long long n = static_cast<long long>(__ldg(cu_q_lens + num_seqs)) * (width / 8);   // 8 values per uint4
+__device__ __forceinline__ void dequant_block(const Q8PrepArgs& a, int s, int lb) {
+  const size_t ob = static_cast<size_t>(s) * a.B + lb;   // block of the copies
+  const int c = __ldg(a.context_lens + s);
+  // lb < B <= max_blocks_per_seq: inside the sequence's table row
+  const int id = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + lb);
+  if (threadIdx.x == 0) a.table_out[ob] = static_cast<int32_t>(ob);
+  if (lb * kBlock >= c) return;
+  const bool live = id >= 0 && id < a.num_blocks;
+  if (!live && threadIdx.x == 0) flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+  const int chunks = a.head_dim / 16;                     // 16-code chunks per row
+  const int per_block = a.num_kv_heads * kBlock * chunks; // chunks per (block, K or V)
+  const size_t src0 = static_cast<size_t>(live ? id : 0) * a.num_kv_heads * kBlock;   // first row of the block
+  const size_t dst0 = ob * a.num_kv_heads * kBlock;
+  const int valid = c - lb * kBlock;                      // rows of the block inside the context
   bool out_of_range = false;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint4 v = src[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
+  for (int base = 0; base < 2 * per_block; base += kUnrollBlock * blockDim.x) {
+    uint4 w[kUnrollBlock];
+    float sc[kUnrollBlock];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if constexpr (TO_HALF) {
-        o[k] = pack_half_sat(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u), out_of_range);
+    for (int u = 0; u < kUnrollBlock; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      const bool is_k = i < per_block;
+      const int j = is_k ? i : i - per_block;
+      const int row = j / chunks;                        // (head, slot) row within the block
+      // rows past the context (stale slots of the last block) are written as zeros
+      if (i < 2 * per_block && live && row % kBlock < valid) {
+        const int8_t* codes = is_k ? a.k_codes : a.v_codes;
+        const float* scales = is_k ? a.k_scales : a.v_scales;
+        w[u] = __ldg(reinterpret_cast<const uint4*>(codes + (src0 + row) * a.head_dim) + (j - row * chunks));
+        sc[u] = __ldg(scales + src0 + row);
       } else {
-        const __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
-        __nv_bfloat162 b = __floats2bfloat162_rn(__low2float(h), __high2float(h));
-        o[k] = *reinterpret_cast<uint32_t*>(&b);
+        w[u] = make_uint4(0u, 0u, 0u, 0u);
+        sc[u] = 0.f;
       }
     }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+    for (int u = 0; u < kUnrollBlock; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i >= 2 * per_block) break;
+      const bool is_k = i < per_block;
+      const int j = is_k ? i : i - per_block;
+      const int row = j / chunks;
+      uint4 lo, hi;
+      widen16(w[u], sc[u], lo, hi, out_of_range);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(is_k ? a.k_out : a.v_out) + (dst0 + row) * a.head_dim) +
+                   2 * (j - row * chunks);
+      dst[0] = lo;
+      dst[1] = hi;
+    }
   }
-  if (out_of_range) flag_status(status, PA_DEV_RANGE);
+  if (out_of_range) flag_status(a.status, PA_DEV_RANGE);
+}
+
+// CTA `cta` of `n_cta`: its share of rows 0 .. cu_q_lens[num_seqs] - 1 of q
+// ([rows][width] bf16, width a multiple of 8) converted to fp16, clamped to
+// fp16's range (reported).
+__device__ __forceinline__ void rows_to_half(const Q8PrepArgs& a, int cta, int n_cta) {
+  const long long n = static_cast<long long>(__ldg(a.cu_q_lens + a.num_seqs)) * (a.width / 8);   // 8 values per uint4
+  const long long step = static_cast<long long>(n_cta) * blockDim.x;
+  bool out_of_range = false;
+  for (long long base = static_cast<long long>(cta) * blockDim.x + threadIdx.x; base < n;
+       base += kUnrollRows * step) {
+    uint4 v[kUnrollRows];
+#pragma unroll
+    for (int u = 0; u < kUnrollRows; ++u) {
+      const long long i = base + u * step;
+      v[u] = i < n ? __ldg(a.q_src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnrollRows; ++u) {
+      const long long i = base + u * step;
+      if (i >= n) break;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        o[k] = pack_half_sat(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u), out_of_range);
+      a.q_dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  if (out_of_range) flag_status(a.status, PA_DEV_RANGE);
+}
+
+// CTAs 0 .. n_cvt - 1 convert q; CTA n_cvt + s * B + lb dequantises block lb
+// of sequence s.  The conversion is a bandwidth-bound stream and the
+// dequantisation a latency-bound one; in one launch each fills the other's
+// idle time.
+__global__ void __launch_bounds__(256) prompt_q8_prep_kernel(const Q8PrepArgs a) {
+  grid_dependency_wait();   // the prompt's rows were appended by the kernel before us
+  const int b = static_cast<int>(blockIdx.x);
+  if (b < a.n_cvt) {
+    rows_to_half(a, b, a.n_cvt);
+  } else {
+    const int u = b - a.n_cvt;
+    dequant_block(a, u / a.B, u - (u / a.B) * a.B);
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_dequant_q8(const void* k_codes, const void* v_codes, const float* k_scales,
-                              const float* v_scales, const int32_t* block_tables, const int32_t* context_lens,
-                              int num_seqs, int max_blocks_per_seq, int num_kv_heads, int head_dim,
-                              int num_blocks, int B, void* k_out, void* v_out, int32_t* table_out, int* status,
-                              cudaStream_t stream) {
-  if (num_seqs == 0 || B == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(B), static_cast<unsigned>(num_seqs));
-  return launch_pdl(dequant_blocks_q8_kernel, grid, dim3(256), 0, stream, static_cast<const int8_t*>(k_codes),
-                    static_cast<const int8_t*>(v_codes), k_scales, v_scales, block_tables, context_lens,
-                    max_blocks_per_seq, num_kv_heads, head_dim, num_blocks, B, static_cast<__half*>(k_out),
-                    static_cast<__half*>(v_out), table_out, status);
-}
-
-cudaError_t launch_convert_rows(const void* src, void* dst, const int32_t* cu_q_lens, int num_seqs, int width,
-                                bool to_half, int* status, cudaStream_t stream) {
+cudaError_t launch_prompt_q8_prep(Q8PrepArgs a, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.B == 0) return cudaSuccess;
   int sms = device_sm_count();
   if (sms <= 0) sms = 152;
-  const dim3 grid(static_cast<unsigned>(4 * sms));
-  const uint4* s = static_cast<const uint4*>(src);
-  uint4* d = static_cast<uint4*>(dst);
-  return to_half ? launch_pdl(convert_rows_kernel<true>, grid, dim3(256), 0, stream, s, d, cu_q_lens, num_seqs, width,
-                              status)
-                 : launch_pdl(convert_rows_kernel<false>, grid, dim3(256), 0, stream, s, d, cu_q_lens, num_seqs, width,
-                              status);
+  a.n_cvt = a.q_src ? 4 * sms : 0;
+  const long long ctas = static_cast<long long>(a.num_seqs) * a.B + a.n_cvt;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_pdl(prompt_q8_prep_kernel, dim3(static_cast<unsigned>(ctas)), dim3(256), 0, stream, a);
 }
 
 }  // namespace pa

@@ -597,11 +597,12 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
 
 namespace {
 
-// The prompt pass over a bf16/fp16 pool once the call has been validated.
+// The prompt pass over a bf16/fp16 pool once the call has been validated: q
+// in the pool's type, the output rows stored as out_dtype.
 int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
                    const int32_t* cu_q_lens, const int32_t* context_lens, float scale, int num_seqs,
-                   int num_q_heads, int max_blocks_per_seq, int max_q_len, const pa_pool_desc* pool, int* status,
-                   void* stream) {
+                   int num_q_heads, int max_blocks_per_seq, int max_q_len, const pa_pool_desc* pool, int out_dtype,
+                   int* status, void* stream) {
   pa::PrefillArgs a{};
   a.out = out;
   a.q = q;
@@ -624,7 +625,8 @@ int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_p
   if ((rc = make_q_map(&qmap, q, pool->dtype, num_q_heads, pool->head_dim,
                        static_cast<long long>(num_seqs) * max_q_len)) != PA_OK)
     return rc;
-  cudaError_t e = pa::launch_prefill_umma(a, pool->dtype, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      pa::launch_prefill_umma(a, pool->dtype, out_dtype, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PA_OK;
 }
@@ -653,16 +655,15 @@ int check_prefill_args(const void* out, const void* q, const int32_t* block_tabl
 
 // Workspace of the INT8 prompt pass: the fp16 copies of the K and V blocks
 // (num_seqs * B blocks, B = blocks of max_context_len), their block table, and
-// for bf16 activations fp16 copies of q and of the output (num_seqs *
-// max_q_len rows at most).
+// for bf16 activations an fp16 copy of q (num_seqs * max_q_len rows at most).
 struct PrefillQ8Ws {
-  size_t k_off, v_off, table_off, q_off, out_off, total;
+  size_t k_off, v_off, table_off, q_off, total;
   int B;
 };
 
 PrefillQ8Ws prefill_q8_ws(int num_seqs, int num_q_heads, int max_q_len, int max_context_len, int act_dtype,
                           const pa_pool_desc* pool) {
-  PrefillQ8Ws w{0, 0, 0, 0, 0, 0, 0};
+  PrefillQ8Ws w{0, 0, 0, 0, 0, 0};
   w.B = (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
   const size_t blocks = static_cast<size_t>(num_seqs) * w.B;
   if (blocks == 0 || max_q_len == 0) return w;
@@ -671,10 +672,11 @@ PrefillQ8Ws prefill_q8_ws(int num_seqs, int num_q_heads, int max_q_len, int max_
   w.k_off = 0;
   w.v_off = align256(pool_bytes);
   w.table_off = w.v_off + align256(pool_bytes);
-  w.q_off = w.table_off + align256(blocks * sizeof(int32_t));
-  w.out_off = w.q_off + (act_dtype == PA_BF16 ? align256(rows_bytes) : 0);
-  w.total = w.out_off + (act_dtype == PA_BF16 ? rows_bytes : 0);
-  if (act_dtype != PA_BF16) w.total = w.table_off + blocks * sizeof(int32_t);
+  w.total = w.table_off + blocks * sizeof(int32_t);
+  if (act_dtype == PA_BF16) {
+    w.q_off = w.table_off + align256(blocks * sizeof(int32_t));
+    w.total = w.q_off + rows_bytes;
+  }
   return w;
 }
 
@@ -699,7 +701,7 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   int* status = status_ptr();
   if (!status) return fail(PA_ERR_CUDA, "no CUDA device / status word unavailable");
   return prefill_launch(out, q, k_pool, v_pool, block_tables, cu_q_lens, context_lens, scale, num_seqs, num_q_heads,
-                        max_blocks_per_seq, max_q_len, pool, status, stream);
+                        max_blocks_per_seq, max_q_len, pool, pool->dtype, status, stream);
 }
 
 size_t pa_prefill_int8_workspace_size(int num_seqs, int num_q_heads, int max_q_len, int max_context_len,
@@ -730,7 +732,7 @@ int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, con
     return rc;
   if (nothing) return PA_OK;
   if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences in one INT8 prompt pass");
-  if (static_cast<long long>(num_seqs) * ((max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE) > 0x7fffffffLL)
+  if (static_cast<long long>(num_seqs) * ((max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE) > 0x7fff0000LL)
     return fail(PA_ERR_UNSUPPORTED, "num_seqs x context blocks too large");
   if (!k_codes || !v_codes || !k_scales || !v_scales) return fail(PA_ERR_INVALID, "null pointer argument");
   if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
@@ -745,28 +747,37 @@ int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, con
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(workspace);
   int32_t* table = reinterpret_cast<int32_t*>(base + ws.table_off);
-  cudaError_t e = pa::launch_dequant_q8(k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, num_seqs,
-                                        max_blocks_per_seq, pool->num_kv_heads, pool->head_dim, pool->num_blocks,
-                                        ws.B, base + ws.k_off, base + ws.v_off, table, status, st);
-  if (e != cudaSuccess) return cuda_fail(e, "INT8 prompt-pass dequantisation launch");
-  // the pass runs in fp16: bf16 queries in, fp16 output back to bf16
+  // the pass runs in fp16: bf16 queries converted on the way in (in the same
+  // launch as the dequantisation), the output rows stored in the
+  // activations' type by the pass
   const bool bf = act_dtype == PA_BF16;
-  const int width = num_q_heads * pool->head_dim;
-  const void* q16 = q;
-  void* out16 = out;
-  if (bf) {
-    q16 = base + ws.q_off;
-    out16 = base + ws.out_off;
-    if ((e = pa::launch_convert_rows(q, base + ws.q_off, cu_q_lens, num_seqs, width, true, status, st)) != cudaSuccess)
-      return cuda_fail(e, "INT8 prompt-pass query conversion launch");
-  }
+  pa::Q8PrepArgs pr{};
+  pr.k_codes = static_cast<const int8_t*>(k_codes);
+  pr.v_codes = static_cast<const int8_t*>(v_codes);
+  pr.k_scales = k_scales;
+  pr.v_scales = v_scales;
+  pr.block_tables = block_tables;
+  pr.context_lens = context_lens;
+  pr.num_seqs = num_seqs;
+  pr.max_blocks_per_seq = max_blocks_per_seq;
+  pr.num_kv_heads = pool->num_kv_heads;
+  pr.head_dim = pool->head_dim;
+  pr.num_blocks = pool->num_blocks;
+  pr.B = ws.B;
+  pr.k_out = base + ws.k_off;
+  pr.v_out = base + ws.v_off;
+  pr.table_out = table;
+  pr.q_src = bf ? static_cast<const uint4*>(q) : nullptr;
+  pr.q_dst = bf ? reinterpret_cast<uint4*>(base + ws.q_off) : nullptr;
+  pr.cu_q_lens = cu_q_lens;
+  pr.width = num_q_heads * pool->head_dim;
+  pr.status = status;
+  cudaError_t e = pa::launch_prompt_q8_prep(pr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "INT8 prompt-pass dequantisation launch");
+  const void* q16 = bf ? static_cast<const void*>(base + ws.q_off) : q;
   const pa_pool_desc fpool{num_seqs * ws.B, pool->num_kv_heads, pool->block_size, pool->head_dim, PA_F16};
-  rc = prefill_launch(out16, q16, base + ws.k_off, base + ws.v_off, table, cu_q_lens, context_lens, scale, num_seqs,
-                      num_q_heads, ws.B, max_q_len, &fpool, status, stream);
-  if (rc != PA_OK || !bf) return rc;
-  if ((e = pa::launch_convert_rows(out16, out, cu_q_lens, num_seqs, width, false, status, st)) != cudaSuccess)
-    return cuda_fail(e, "INT8 prompt-pass output conversion launch");
-  return PA_OK;
+  return prefill_launch(out, q16, base + ws.k_off, base + ws.v_off, table, cu_q_lens, context_lens, scale, num_seqs,
+                        num_q_heads, ws.B, max_q_len, &fpool, act_dtype, status, stream);
 }
 
 int pa_append_kv_int8(void* k_codes, void* v_codes, float* k_scales, float* v_scales,

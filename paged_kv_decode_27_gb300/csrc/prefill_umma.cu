@@ -119,7 +119,10 @@ __device__ __forceinline__ int key_tiles(int c, int n, int t) {
 
 }  // namespace
 
-template <typename T, int D>
+// T: the type of q, of the pool and of the products' operands; TO: the type
+// the output rows are stored in (T, or bf16 for an fp16 pass over bf16
+// activations).
+template <typename T, typename TO, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const __grid_constant__ CUtensorMap qmap, const PrefillArgs a) {
@@ -642,7 +645,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int lr = it.t * kRows + r;
-      T* orow = static_cast<T*>(a.out) + ((static_cast<size_t>(it.q0) + lr) * H + it.h + g) * D;
+      TO* orow = static_cast<TO*>(a.out) + ((static_cast<size_t>(it.q0) + lr) * H + it.h + g) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
@@ -651,10 +654,10 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 v;
-            v.x = Mma<T>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
-            v.y = Mma<T>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
-            v.z = Mma<T>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
-            v.w = Mma<T>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
+            v.x = Mma<TO>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
+            v.y = Mma<TO>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
+            v.z = Mma<TO>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
+            v.w = Mma<TO>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
             reinterpret_cast<uint4*>(orow + cc * 32)[e] = v;
           }
         }
@@ -679,11 +682,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 }
 
 namespace {
-template <typename T, int D>
+template <typename T, typename TO, int D>
 cudaError_t launch_umma_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const CUtensorMap& qmap, cudaStream_t stream) {
   const int smem = UmmaLayout<D>::SMEM + 1024;
-  auto kern = prefill_umma_kernel<T, D>;
+  auto kern = prefill_umma_kernel<T, TO, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM, or fewer when there are fewer items
@@ -696,16 +699,20 @@ cudaError_t launch_umma_t(const PrefillArgs& a, const CUtensorMap& kmap, const C
   if (ctas <= 0) return cudaSuccess;
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, kmap, vmap, qmap, a);
 }
+
+template <typename T, typename TO>
+cudaError_t launch_umma_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const CUtensorMap& qmap, cudaStream_t stream) {
+  return a.head_dim == 128 ? launch_umma_t<T, TO, 128>(a, kmap, vmap, qmap, stream)
+                           : launch_umma_t<T, TO, 64>(a, kmap, vmap, qmap, stream);
+}
 }  // namespace
 
-cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, const CUtensorMap& kmap,
+cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, int out_dtype, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& qmap, cudaStream_t stream) {
-  if (dtype == PA_BF16) {
-    return a.head_dim == 128 ? launch_umma_t<__nv_bfloat16, 128>(a, kmap, vmap, qmap, stream)
-                             : launch_umma_t<__nv_bfloat16, 64>(a, kmap, vmap, qmap, stream);
-  }
-  return a.head_dim == 128 ? launch_umma_t<__half, 128>(a, kmap, vmap, qmap, stream)
-                           : launch_umma_t<__half, 64>(a, kmap, vmap, qmap, stream);
+  if (dtype == PA_BF16) return launch_umma_d<__nv_bfloat16, __nv_bfloat16>(a, kmap, vmap, qmap, stream);
+  if (out_dtype == PA_BF16) return launch_umma_d<__half, __nv_bfloat16>(a, kmap, vmap, qmap, stream);
+  return launch_umma_d<__half, __half>(a, kmap, vmap, qmap, stream);
 }
 
 }  // namespace pa

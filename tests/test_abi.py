@@ -109,8 +109,9 @@ def test_int8_prefill_validates_on_the_host(lib):
     """The INT8 prompt pass: the pool must be INT8 with a bf16/fp16 act_dtype,
     the workspace present and large enough.  The workspace is the fp16 K and V
     copies of num_seqs x ceil(max_context_len / 16) blocks and their int32
-    block table (each part 256-byte aligned), and for bf16 activations fp16
-    copies of num_seqs x max_q_len rows of q and of the output."""
+    block table (each part 256-byte aligned), and for bf16 activations an
+    fp16 copy of num_seqs x max_q_len rows of q (the pass stores the output
+    rows as bf16 itself)."""
     f = ctypes.c_void_p(FAKE)
     i8 = _desc(dt=B.PA_I8)
     al = lambda n: ((n + 255) // 256) * 256
@@ -119,7 +120,7 @@ def test_int8_prefill_validates_on_the_host(lib):
     f16 = lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_F16, ctypes.byref(i8))
     assert f16 == 2 * al(pool) + 2 * 4 * 4
     size = lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_BF16, ctypes.byref(i8))
-    assert size == 2 * al(pool) + al(2 * 4 * 4) + al(rows) + rows
+    assert size == 2 * al(pool) + al(2 * 4 * 4) + rows
     assert lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_BF16, ctypes.byref(_desc(dt=B.PA_BF16))) == 0
     assert lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_F32, ctypes.byref(i8)) == 0
     call = lambda desc, act=B.PA_BF16, ws=f, wsb=size, maxq=64, maxc=64, S=2: lib.pa_prefill_attention_int8(
