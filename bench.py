@@ -685,7 +685,7 @@ def measure_workload(name, pa, W, torch, dev, reps, warmup, partition=0, flush=N
     pws = None
     if wl.prompt_lens and wl.kv_int8:   # the INT8 prompt pass dequantises into its workspace
         mp = max(wl.prompt_lens)
-        pws = torch.empty(max(1, pa.pa_prefill_int8_workspace_size(len(wl.prompt_lens), hq, mp, mp, kp, wl.dtype)),
+        pws = torch.empty(max(1, pa.pa_prefill_int8_workspace_size(len(wl.prompt_lens), mp, kp)),
                           dtype=torch.uint8, device=dev)
     flush = flush or l2_flusher(torch, dev)
     stream = torch.cuda.current_stream()

@@ -360,22 +360,24 @@ PA_API int pa_verify_attention_int8(void* out, const void* q, const void* k_code
  * context_lens[s] positions are first dequantised into `workspace` (every
  * x_hat rounded once to fp16, 11 significant bits, in the float pool layout),
  * and the fp16 prompt pass runs over those copies; bf16 queries are converted
- * to fp16 (exactly, within fp16's range) and the pass stores its output rows
- * as bf16.
+ * to fp16 in shared memory by the pass (exactly, within fp16's range) and the
+ * output rows stored as bf16.
  *   out, q   : act_dtype [cu_q_lens[num_seqs]][num_q_heads][D]
  *   the other arguments as pa_prefill_attention; pool->dtype = PA_I8
  *   workspace: device, 16-byte aligned, >= pa_prefill_int8_workspace_size()
  *              bytes, owned by the caller, its contents scratch: the fp16 K
  *              and V copies of num_seqs x ceil(max_context_len / 16) blocks
- *              and their block table, and for bf16 activations an fp16 copy
- *              of num_seqs x max_q_len rows of q.
+ *              (each 256-byte aligned) and their int32 block table.
  * Errors as pa_prefill_attention, plus PA_ERR_INVALID for a missing or small
  * workspace and PA_ERR_UNSUPPORTED past 65535 sequences.  A block id outside
  * the pool sets PA_DEV_BAD_BLOCK_ID and its keys read as zeros; a cache or
- * query value past fp16's range (|x| > 65504) is clamped and sets PA_DEV_RANGE.
+ * query value past fp16's range (|x| > 65504 for a dequantised cache value,
+ * |q| >= 65536 for a bf16 query, inf and NaN included) is clamped to +-65504
+ * and sets PA_DEV_RANGE.
+ * pa_prefill_int8_workspace_size returns 0 (and sets the last error) for a
+ * pool that is not INT8 or negative sizes.
  */
-PA_API size_t pa_prefill_int8_workspace_size(int num_seqs, int num_q_heads, int max_q_len,
-                                             int max_context_len, int act_dtype,
+PA_API size_t pa_prefill_int8_workspace_size(int num_seqs, int max_context_len,
                                              const pa_pool_desc* pool);
 PA_API int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes,
                                      const void* v_codes, const float* k_scales,

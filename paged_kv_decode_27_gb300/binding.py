@@ -122,7 +122,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_verify_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
                                            i32, pdesc, vp, sz, vp]
     L.pa_prefill_int8_workspace_size.restype = sz
-    L.pa_prefill_int8_workspace_size.argtypes = [i32, i32, i32, i32, i32, pdesc]
+    L.pa_prefill_int8_workspace_size.argtypes = [i32, i32, pdesc]
     L.pa_prefill_attention_int8.restype = i32
     L.pa_prefill_attention_int8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, i32, i32,
                                             pdesc, vp, sz, vp]
@@ -487,14 +487,12 @@ def pa_verify_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch.
                                       _act(q), ctypes.byref(desc), _ptr(workspace), int(ws_bytes),
                                       _stream(stream)))
 
-def pa_prefill_int8_workspace_size(num_seqs: int, num_q_heads: int, max_q_len: int, max_context_len: int,
-                                   k_codes: torch.Tensor, act_dtype: torch.dtype) -> int:
+def pa_prefill_int8_workspace_size(num_seqs: int, max_context_len: int, k_codes: torch.Tensor) -> int:
     """Bytes of workspace pa_prefill_attention_int8 needs (k_codes: the int8
-    pool; act_dtype: torch.bfloat16 or torch.float16)."""
+    pool)."""
     L = load_library()
     desc = pool_desc(k_codes)
-    n = L.pa_prefill_int8_workspace_size(int(num_seqs), int(num_q_heads), int(max_q_len), int(max_context_len),
-                                         _DTYPES[act_dtype], ctypes.byref(desc))
+    n = L.pa_prefill_int8_workspace_size(int(num_seqs), int(max_context_len), ctypes.byref(desc))
     msg = pa_last_error()
     if msg:
         raise PaError(PA_ERR_INVALID, msg)
@@ -520,7 +518,7 @@ def pa_prefill_attention_int8(out: torch.Tensor, q: torch.Tensor, k_codes: torch
           "block_tables must be int32 [S][max_blocks]")
     L = load_library()
     if workspace is None:
-        need = pa_prefill_int8_workspace_size(S, int(q.shape[1]), max_q_len, max_context_len, k_codes, q.dtype)
+        need = pa_prefill_int8_workspace_size(S, max_context_len, k_codes)
         if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

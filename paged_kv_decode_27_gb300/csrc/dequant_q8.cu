@@ -18,16 +18,14 @@
 // blocks past it are not written (the prompt pass never reads them); a block id
 // outside the pool is reported and its copy holds zeros.
 //
-// bf16 queries are converted to fp16 for the pass (exact for |q| in fp16's
-// normal range: bf16 carries 8 significant bits); the pass stores its output
-// rows as bf16 itself.
+// bf16 queries are converted to fp16 by the pass itself (in shared memory,
+// exact for |q| in fp16's normal range: bf16 carries 8 significant bits),
+// which also stores its output rows as bf16.
 //
-// One launch does both: a CTA per (sequence, block), where a thread widens 16
-// codes of a row (one 16-byte load, two 16-byte stores), eight such chunks
-// with their loads issued together, and 4 x SMs CTAs streaming the query
-// conversion.  The dequantisation waits on load latency (context length and
-// block id, then the codes), the conversion on bandwidth, so each runs in the
-// other's idle time.
+// One CTA per (sequence, block); a thread widens 16 codes of a row (one
+// 16-byte load, two 16-byte stores), eight such chunks with their loads
+// issued together, and the context length and block id are read together:
+// a CTA waits on two load latencies.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -63,13 +61,9 @@ __device__ __forceinline__ void widen16(const uint4 w, float s, uint4& lo, uint4
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// One CTA dequantises one (sequence, block): every load of a thread's chunks
-// (kUnrollBlock of them) is issued before the first is used, and the context
-// length and block id are read together, so a CTA waits on two load latencies.
-constexpr int kUnrollBlock = 8;
-constexpr int kUnrollRows = 4;
+constexpr int kUnrollBlock = 8;   // chunks a thread loads before widening the first
 
-__device__ __forceinline__ void dequant_block(const Q8PrepArgs& a, int s, int lb) {
+__device__ __forceinline__ void dequant_block(const DequantQ8Args& a, int s, int lb) {
   const size_t ob = static_cast<size_t>(s) * a.B + lb;   // block of the copies
   const int c = __ldg(a.context_lens + s);
   // lb < B <= max_blocks_per_seq: inside the sequence's table row
@@ -122,61 +116,17 @@ __device__ __forceinline__ void dequant_block(const Q8PrepArgs& a, int s, int lb
   if (out_of_range) flag_status(a.status, PA_DEV_RANGE);
 }
 
-// CTA `cta` of `n_cta`: its share of rows 0 .. cu_q_lens[num_seqs] - 1 of q
-// ([rows][width] bf16, width a multiple of 8) converted to fp16, clamped to
-// fp16's range (reported).
-__device__ __forceinline__ void rows_to_half(const Q8PrepArgs& a, int cta, int n_cta) {
-  const long long n = static_cast<long long>(__ldg(a.cu_q_lens + a.num_seqs)) * (a.width / 8);   // 8 values per uint4
-  const long long step = static_cast<long long>(n_cta) * blockDim.x;
-  bool out_of_range = false;
-  for (long long base = static_cast<long long>(cta) * blockDim.x + threadIdx.x; base < n;
-       base += kUnrollRows * step) {
-    uint4 v[kUnrollRows];
-#pragma unroll
-    for (int u = 0; u < kUnrollRows; ++u) {
-      const long long i = base + u * step;
-      v[u] = i < n ? __ldg(a.q_src + i) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnrollRows; ++u) {
-      const long long i = base + u * step;
-      if (i >= n) break;
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        o[k] = pack_half_sat(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u), out_of_range);
-      a.q_dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-  if (out_of_range) flag_status(a.status, PA_DEV_RANGE);
-}
-
-// CTAs 0 .. n_cvt - 1 convert q; CTA n_cvt + s * B + lb dequantises block lb
-// of sequence s.  The conversion is a bandwidth-bound stream and the
-// dequantisation a latency-bound one; in one launch each fills the other's
-// idle time.
-__global__ void __launch_bounds__(256) prompt_q8_prep_kernel(const Q8PrepArgs a) {
+__global__ void __launch_bounds__(256) dequant_blocks_q8_kernel(const DequantQ8Args a) {
   grid_dependency_wait();   // the prompt's rows were appended by the kernel before us
-  const int b = static_cast<int>(blockIdx.x);
-  if (b < a.n_cvt) {
-    rows_to_half(a, b, a.n_cvt);
-  } else {
-    const int u = b - a.n_cvt;
-    dequant_block(a, u / a.B, u - (u / a.B) * a.B);
-  }
+  dequant_block(a, static_cast<int>(blockIdx.y), static_cast<int>(blockIdx.x));
 }
 
 }  // namespace
 
-cudaError_t launch_prompt_q8_prep(Q8PrepArgs a, cudaStream_t stream) {
+cudaError_t launch_dequant_q8(const DequantQ8Args& a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.B == 0) return cudaSuccess;
-  int sms = device_sm_count();
-  if (sms <= 0) sms = 152;
-  a.n_cvt = a.q_src ? 4 * sms : 0;
-  const long long ctas = static_cast<long long>(a.num_seqs) * a.B + a.n_cvt;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  return launch_pdl(prompt_q8_prep_kernel, dim3(static_cast<unsigned>(ctas)), dim3(256), 0, stream, a);
+  return launch_pdl(dequant_blocks_q8_kernel, dim3(static_cast<unsigned>(a.B), static_cast<unsigned>(a.num_seqs)),
+                    dim3(256), 0, stream, a);
 }
 
 }  // namespace pa

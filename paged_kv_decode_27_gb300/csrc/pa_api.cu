@@ -598,10 +598,11 @@ int pa_verify_attention(void* out, const void* q, const void* k_pool, const void
 namespace {
 
 // The prompt pass over a bf16/fp16 pool once the call has been validated: q
-// in the pool's type, the output rows stored as out_dtype.
+// and the output rows in act_dtype (the pool's type, or bf16 over an fp16
+// pool).
 int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
                    const int32_t* cu_q_lens, const int32_t* context_lens, float scale, int num_seqs,
-                   int num_q_heads, int max_blocks_per_seq, int max_q_len, const pa_pool_desc* pool, int out_dtype,
+                   int num_q_heads, int max_blocks_per_seq, int max_q_len, const pa_pool_desc* pool, int act_dtype,
                    int* status, void* stream) {
   pa::PrefillArgs a{};
   a.out = out;
@@ -622,11 +623,11 @@ int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_p
   int rc;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
   if ((rc = pool_map(&vmap, v_pool, pool)) != PA_OK) return rc;
-  if ((rc = make_q_map(&qmap, q, pool->dtype, num_q_heads, pool->head_dim,
+  if ((rc = make_q_map(&qmap, q, act_dtype, num_q_heads, pool->head_dim,
                        static_cast<long long>(num_seqs) * max_q_len)) != PA_OK)
     return rc;
   cudaError_t e =
-      pa::launch_prefill_umma(a, pool->dtype, out_dtype, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
+      pa::launch_prefill_umma(a, pool->dtype, act_dtype, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PA_OK;
 }
@@ -654,29 +655,22 @@ int check_prefill_args(const void* out, const void* q, const int32_t* block_tabl
 }
 
 // Workspace of the INT8 prompt pass: the fp16 copies of the K and V blocks
-// (num_seqs * B blocks, B = blocks of max_context_len), their block table, and
-// for bf16 activations an fp16 copy of q (num_seqs * max_q_len rows at most).
+// (num_seqs * B blocks, B = blocks of max_context_len) and their block table.
 struct PrefillQ8Ws {
-  size_t k_off, v_off, table_off, q_off, total;
+  size_t k_off, v_off, table_off, total;
   int B;
 };
 
-PrefillQ8Ws prefill_q8_ws(int num_seqs, int num_q_heads, int max_q_len, int max_context_len, int act_dtype,
-                          const pa_pool_desc* pool) {
-  PrefillQ8Ws w{0, 0, 0, 0, 0, 0};
+PrefillQ8Ws prefill_q8_ws(int num_seqs, int max_context_len, const pa_pool_desc* pool) {
+  PrefillQ8Ws w{0, 0, 0, 0, 0};
   w.B = (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
   const size_t blocks = static_cast<size_t>(num_seqs) * w.B;
-  if (blocks == 0 || max_q_len == 0) return w;
+  if (blocks == 0) return w;
   const size_t pool_bytes = blocks * pool->num_kv_heads * PA_BLOCK_SIZE * pool->head_dim * 2;
-  const size_t rows_bytes = static_cast<size_t>(num_seqs) * max_q_len * num_q_heads * pool->head_dim * 2;
   w.k_off = 0;
   w.v_off = align256(pool_bytes);
   w.table_off = w.v_off + align256(pool_bytes);
   w.total = w.table_off + blocks * sizeof(int32_t);
-  if (act_dtype == PA_BF16) {
-    w.q_off = w.table_off + align256(blocks * sizeof(int32_t));
-    w.total = w.q_off + rows_bytes;
-  }
   return w;
 }
 
@@ -704,16 +698,18 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
                         max_blocks_per_seq, max_q_len, pool, pool->dtype, status, stream);
 }
 
-size_t pa_prefill_int8_workspace_size(int num_seqs, int num_q_heads, int max_q_len, int max_context_len,
-                                      int act_dtype, const pa_pool_desc* pool) {
+size_t pa_prefill_int8_workspace_size(int num_seqs, int max_context_len, const pa_pool_desc* pool) {
   t_err.clear();
   if (check_pool(pool) != PA_OK) return 0;
-  if (check_int8(pool, act_dtype) != PA_OK) return 0;
-  if (num_seqs < 0 || num_q_heads < 1 || max_q_len < 0 || max_context_len < 0) {
-    fail(PA_ERR_INVALID, "num_seqs, max_q_len and max_context_len must be >= 0, num_q_heads >= 1");
+  if (pool->dtype != PA_I8) {
+    fail(PA_ERR_INVALID, "the INT8 prompt pass needs an INT8 pool");
     return 0;
   }
-  return prefill_q8_ws(num_seqs, num_q_heads, max_q_len, max_context_len, act_dtype, pool).total;
+  if (num_seqs < 0 || max_context_len < 0) {
+    fail(PA_ERR_INVALID, "num_seqs and max_context_len must be >= 0");
+    return 0;
+  }
+  return prefill_q8_ws(num_seqs, max_context_len, pool).total;
 }
 
 int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, const void* v_codes,
@@ -732,12 +728,12 @@ int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, con
     return rc;
   if (nothing) return PA_OK;
   if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences in one INT8 prompt pass");
-  if (static_cast<long long>(num_seqs) * ((max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE) > 0x7fff0000LL)
+  if (static_cast<long long>(num_seqs) * ((max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE) > 0x7fffffffLL)
     return fail(PA_ERR_UNSUPPORTED, "num_seqs x context blocks too large");
   if (!k_codes || !v_codes || !k_scales || !v_scales) return fail(PA_ERR_INVALID, "null pointer argument");
   if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) || !aligned16(v_scales))
     return fail(PA_ERR_INVALID, "codes and scales must be 16-byte aligned");
-  const PrefillQ8Ws ws = prefill_q8_ws(num_seqs, num_q_heads, max_q_len, max_context_len, act_dtype, pool);
+  const PrefillQ8Ws ws = prefill_q8_ws(num_seqs, max_context_len, pool);
   if (!workspace) return fail(PA_ERR_INVALID, "workspace of %zu bytes required, got NULL", ws.total);
   if (workspace_bytes < ws.total)
     return fail(PA_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, ws.total);
@@ -747,36 +743,29 @@ int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, con
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(workspace);
   int32_t* table = reinterpret_cast<int32_t*>(base + ws.table_off);
-  // the pass runs in fp16: bf16 queries converted on the way in (in the same
-  // launch as the dequantisation), the output rows stored in the
-  // activations' type by the pass
-  const bool bf = act_dtype == PA_BF16;
-  pa::Q8PrepArgs pr{};
-  pr.k_codes = static_cast<const int8_t*>(k_codes);
-  pr.v_codes = static_cast<const int8_t*>(v_codes);
-  pr.k_scales = k_scales;
-  pr.v_scales = v_scales;
-  pr.block_tables = block_tables;
-  pr.context_lens = context_lens;
-  pr.num_seqs = num_seqs;
-  pr.max_blocks_per_seq = max_blocks_per_seq;
-  pr.num_kv_heads = pool->num_kv_heads;
-  pr.head_dim = pool->head_dim;
-  pr.num_blocks = pool->num_blocks;
-  pr.B = ws.B;
-  pr.k_out = base + ws.k_off;
-  pr.v_out = base + ws.v_off;
-  pr.table_out = table;
-  pr.q_src = bf ? static_cast<const uint4*>(q) : nullptr;
-  pr.q_dst = bf ? reinterpret_cast<uint4*>(base + ws.q_off) : nullptr;
-  pr.cu_q_lens = cu_q_lens;
-  pr.width = num_q_heads * pool->head_dim;
-  pr.status = status;
-  cudaError_t e = pa::launch_prompt_q8_prep(pr, st);
+  // the pass runs in fp16 over the copies; bf16 queries are converted in
+  // shared memory and the output rows stored as bf16 by the pass itself
+  pa::DequantQ8Args dq{};
+  dq.k_codes = static_cast<const int8_t*>(k_codes);
+  dq.v_codes = static_cast<const int8_t*>(v_codes);
+  dq.k_scales = k_scales;
+  dq.v_scales = v_scales;
+  dq.block_tables = block_tables;
+  dq.context_lens = context_lens;
+  dq.num_seqs = num_seqs;
+  dq.max_blocks_per_seq = max_blocks_per_seq;
+  dq.num_kv_heads = pool->num_kv_heads;
+  dq.head_dim = pool->head_dim;
+  dq.num_blocks = pool->num_blocks;
+  dq.B = ws.B;
+  dq.k_out = base + ws.k_off;
+  dq.v_out = base + ws.v_off;
+  dq.table_out = table;
+  dq.status = status;
+  cudaError_t e = pa::launch_dequant_q8(dq, st);
   if (e != cudaSuccess) return cuda_fail(e, "INT8 prompt-pass dequantisation launch");
-  const void* q16 = bf ? static_cast<const void*>(base + ws.q_off) : q;
   const pa_pool_desc fpool{num_seqs * ws.B, pool->num_kv_heads, pool->block_size, pool->head_dim, PA_F16};
-  return prefill_launch(out, q16, base + ws.k_off, base + ws.v_off, table, cu_q_lens, context_lens, scale, num_seqs,
+  return prefill_launch(out, q, base + ws.k_off, base + ws.v_off, table, cu_q_lens, context_lens, scale, num_seqs,
                         num_q_heads, ws.B, max_q_len, &fpool, act_dtype, status, stream);
 }
 

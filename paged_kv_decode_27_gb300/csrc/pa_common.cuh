@@ -505,13 +505,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Byte offset of element column `col` (2-byte elements) of row `row` inside a
-// TMA box of [rows][64] elements written with 128-byte swizzling: each
-// 128-byte row's 16-byte chunks are permuted by XOR with (row % 8).
+// 16-byte shared-memory load / store at a 16-byte aligned address
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
@@ -522,6 +523,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// Byte offset of 16-byte chunk `chunk16` of row `row` inside a TMA box of
+// 128-byte rows written with 128-byte swizzling: each row's chunks are
+// permuted by XOR with (row % 8).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
   return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
 }

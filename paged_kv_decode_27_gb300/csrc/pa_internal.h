@@ -124,17 +124,13 @@ struct CopyArrays {
 cudaError_t launch_copy_blocks(const CopyArrays& arrs, int num_arrays, const int32_t* pairs, int num_pairs,
                                int num_blocks, int* status, cudaStream_t stream);
 
-// The preparation of a prompt pass over an INT8 cache, in one launch.
-//  * The blocks of each sequence's first context_lens[s] positions,
-//    dequantised to fp16 into a pool of num_seqs * B blocks (k_out, v_out),
-//    sequence s owning blocks s * B .. s * B + B - 1, with the block table
-//    table_out[s][lb] = s * B + lb.  A block id outside the pool sets
-//    PA_DEV_BAD_BLOCK_ID and gives zeros; a value past fp16's range is clamped
-//    and sets PA_DEV_RANGE.
-//  * When q_src is not null: rows 0 .. cu_q_lens[num_seqs] - 1 of bf16 q
-//    ([rows][width], width a multiple of 8) converted to fp16 into q_dst
-//    (clamped, PA_DEV_RANGE).
-struct Q8PrepArgs {
+// The blocks of each sequence's first context_lens[s] positions of an INT8
+// cache, dequantised to fp16 into a pool of num_seqs * B blocks (k_out,
+// v_out), sequence s owning blocks s * B .. s * B + B - 1, with the block
+// table table_out[s][lb] = s * B + lb.  A block id outside the pool sets
+// PA_DEV_BAD_BLOCK_ID and gives zeros; a value past fp16's range is clamped
+// and sets PA_DEV_RANGE.
+struct DequantQ8Args {
   const int8_t* k_codes;
   const int8_t* v_codes;
   const float* k_scales;
@@ -145,20 +141,15 @@ struct Q8PrepArgs {
   void* k_out;   // fp16
   void* v_out;   // fp16
   int32_t* table_out;
-  const uint4* q_src;
-  uint4* q_dst;
-  const int32_t* cu_q_lens;
-  int width;
-  int n_cvt;   // set by the launcher
   int* status;
 };
-cudaError_t launch_prompt_q8_prep(Q8PrepArgs a, cudaStream_t stream);
+cudaError_t launch_dequant_q8(const DequantQ8Args& a, cudaStream_t stream);
 
 // Causal prefill on tcgen05 with tensor-memory accumulators (bf16/fp16, D in {64, 128}).
-// dtype: q, the pools and the products; out_dtype: the output rows (dtype, or
-// PA_BF16 over an fp16 pass).
+// dtype: the pools and the products; act_dtype: q and the output rows (dtype,
+// or PA_BF16 over an fp16 pool: the pass converts q in shared memory).
 // qmap: the queries as (D, H, rows) in 128-row x 64-column boxes (whole query tiles only).
-cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, int out_dtype, const CUtensorMap& kmap,
+cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, int act_dtype, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& qmap, cudaStream_t stream);
 
 

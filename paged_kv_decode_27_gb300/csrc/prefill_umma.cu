@@ -48,7 +48,10 @@
 // Warps (384 threads, three warpgroups that re-balance their registers with
 // setmaxnreg):
 //   0-3 / 4-7  softmax of tile A / B (thread r owns query row r), and at the
-//              end of an item the epilogue: normalise O and store the rows;
+//              end of an item the epilogue: normalise O and store the rows
+//              (for bf16 queries over an fp16 pool, also the in-place
+//              conversion of the tile's next Q, done while the item's last
+//              PV runs, so that the next item's S overlaps the epilogue);
 //   8 / 10     TMA producers of the K ring / the V ring (pool rows through the
 //              block table);
 //   9          MMA issuer of both tiles (lane 0 alone), in the interleaved
@@ -119,21 +122,22 @@ __device__ __forceinline__ int key_tiles(int c, int n, int t) {
 
 }  // namespace
 
-// T: the type of q, of the pool and of the products' operands; TO: the type
-// the output rows are stored in (T, or bf16 for an fp16 pass over bf16
-// activations).
-template <typename T, typename TO, int D>
+// T: the type of the pool and of the products' operands; TA: the type of q
+// and of the output rows (T, or bf16 for an fp16 pass over bf16 activations:
+// the query loader then converts each Q tile in shared memory).
+template <typename T, typename TA, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const __grid_constant__ CUtensorMap qmap, const PrefillArgs a) {
   using L = UmmaLayout<D>;
   constexpr int NBOX = L::NBOX;
   constexpr bool kBf16 = !std::is_same<T, __half>::value;
+  constexpr bool kCvtQ = !std::is_same<T, TA>::value;   // bf16 queries into an fp16 pass
 
   extern __shared__ uint8_t smem_raw[];
   // k_full[2] k_empty[2] v_full[3] v_empty[3] | s_full[2] p_full[2] pv_done[2] o_free[2] |
-  // q_full[2] q_empty[2] | mma_final
-  __shared__ __align__(8) uint64_t bars[23];
+  // q_full[2] q_empty[2] | mma_final | q_raw[2]
+  __shared__ __align__(8) uint64_t bars[kCvtQ ? 25 : 23];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
   __shared__ int n_pairs_sh;
@@ -165,6 +169,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   auto q_full = [&](int g) { return bar0 + 144u + 8u * g; };
   auto q_empty = [&](int g) { return bar0 + 160u + 8u * g; };
   auto mma_final = [&](int g) { return bar0 + 176u + 8u * g; };
+  auto q_raw = [&](int g) { return bar0 + 184u + 8u * g; };   // a Q tile landed, before its conversion
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesK; ++i) {
@@ -180,8 +185,9 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       mbar_init(p_full(g), 4);
       mbar_init(pv_done(g), 1);
       mbar_init(o_free(g), 4);
-      mbar_init(q_full(g), 1);
+      mbar_init(q_full(g), kCvtQ ? 4 : 1);   // the TMA, or the tile's four softmax warps after the conversion
       mbar_init(q_empty(g), 1);
+      if (kCvtQ) mbar_init(q_raw(g), 1);
     }
     mbar_init(mma_final(0), 1);
     fence_barrier_init();
@@ -476,10 +482,13 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // Q rows of the item's tiles -> shared memory in the 128-byte-swizzled
       // K-major layout: a whole tile by TMA (the 3-D query map), the prompt's
       // last partial tile by cp.async with the rows past the prompt zeroed.
+      // bf16 queries for an fp16 pass land on q_raw instead: the tile's
+      // softmax threads convert them in place and complete q_full.
       constexpr int CH = D / 8;   // 16-byte chunks per row
       const uint64_t policy_q = l2_policy_evict_first();   // each query tile is read once
       bool ok = true;
       uint32_t itc = 0;
+      uint32_t tma_uses[2] = {0u, 0u};   // q_raw phases this warp started (convert mode)
       long long k = 0;
       Item it;
       while (ok && find_item(k, it)) {
@@ -497,36 +506,43 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           if ((it.t + 1) * kRows <= it.n) {
             // a whole tile: NBOX boxes of 128 rows x 64 columns, by TMA
             if (lane == 0) {
-              mbar_arrive_expect_tx(q_full(g), L::Q_BYTES);
+              const uint32_t bar = kCvtQ ? q_raw(g) : q_full(g);
+              mbar_arrive_expect_tx(bar, L::Q_BYTES);
               for (int h = 0; h < NBOX; ++h)
-                tma_load_3d(qbase + h * L::HALF_Q, &qmap, h * 64, it.h + g, it.q0 + it.t * kRows, q_full(g),
-                            policy_q);
+                tma_load_3d(qbase + h * L::HALF_Q, &qmap, h * 64, it.h + g, it.q0 + it.t * kRows, bar, policy_q);
             }
             __syncwarp();
           } else {
             // the prompt's last, partial tile (whose rows past the prompt may
             // lie past the caller's buffer): cp.async of the rows that exist
-            const T* qh = static_cast<const T*>(a.q) + static_cast<size_t>(it.h + g) * D;
+            const TA* qh = static_cast<const TA*>(a.q) + static_cast<size_t>(it.h + g) * D;
             for (int idx = lane; idx < kRows * CH; idx += 32) {
               const int r = idx / CH;
               const int cc = idx - r * CH;
               const int lr = it.t * kRows + r;
               const bool in = lr < it.n;
-              const T* src = in ? qh + (static_cast<size_t>(it.q0) + lr) * H * D + cc * 8 : qh;
+              const TA* src = in ? qh + (static_cast<size_t>(it.q0) + lr) * H * D + cc * 8 : qh;
               const uint32_t dst = qbase + (cc >> 3) * L::HALF_Q + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
               cp_async_16(dst, src, in ? 16u : 0u);
             }
             cp_async_wait_all();
-            fence_proxy_async_smem();   // the MMAs (async proxy) read what these copies wrote
+            if constexpr (!kCvtQ) fence_proxy_async_smem();   // the MMAs (async proxy) read what these copies wrote
             __syncwarp();
-            if (lane == 0) mbar_arrive(q_full(g));
+            if (lane == 0) mbar_arrive(kCvtQ ? q_raw(g) : q_full(g));
           }
+          if constexpr (kCvtQ) ++tma_uses[g];
         }
         if (!ok) break;
         ++itc;
         ++k;
       }
       if (!ok) abort_sh = 1;
+      if (kCvtQ && lane == 0) {
+        // the last copy of each tile may still be in flight when the softmax
+        // warps have stopped waiting for it (an abort): let it land
+        for (int g = 0; g < NT; ++g)
+          if (tma_uses[g] > 0) mbar_wait_bounded(q_raw(g), (tma_uses[g] - 1) & 1u, 100000000ull);
+      }
     }
     teardown();
   } else if (warp < 4 || paired) {
@@ -548,10 +564,51 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     // S_g(j) of the last tile completes after every earlier product of the
     // single issuing thread (PV(j - 1) of both tiles included)
     const bool releaser = g == NT - 1 && (warp & 3) == 0 && lane == 0;
+    // bf16 queries for an fp16 pass: the tile's 128 threads convert its Q
+    // tile in place once it has landed (q_raw) and complete q_full -- the
+    // first item's before its loop, each next item's while the current
+    // item's last PV runs, so the next S can start during the epilogue.  A
+    // bf16 exponent field of 143 or more (|x| >= 2^16, inf, NaN) carries
+    // (256 - 143) into its half's top bit, which `range` collects; such
+    // values saturate to +-65504.
+    uint32_t range = 0;
+    auto convert_q = [&](uint32_t use) -> bool {
+      const bool landed = !abort_sh && mbar_wait_bounded(q_raw(g), use & 1u);
+      if (!__all_sync(0xffffffffu, landed)) return false;
+      const uint32_t qbase = sQ + g * L::Q_BYTES;
+#pragma unroll 4
+      for (int off = r * 16; off < L::Q_BYTES; off += kRows * 16) {
+        const uint4 v = lds128(qbase + off);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          range |= (w[e] & 0x7f807f80u) + 0x38803880u;
+          asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+              : "=r"(o[e])
+              : "f"(__uint_as_float(w[e] & 0xffff0000u)), "f"(__uint_as_float(w[e] << 16)));
+        }
+        sts128(qbase + off, o[0], o[1], o[2], o[3]);
+      }
+      fence_proxy_async_smem();   // the MMAs (async proxy) read what these threads wrote
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full(g));
+      return true;
+    };
     bool ok = true;
     long long k = 0;
     Item it;
+    if constexpr (kCvtQ) {
+      long long k0 = 0;
+      if (find_item(k0, it)) ok = convert_q(0);
+    }
     while (ok && find_item(k, it)) {
+      bool more = false;   // convert mode: another item follows this one
+      if constexpr (kCvtQ) {
+        long long kn = k + 1;
+        Item nx;
+        more = find_item(kn, nx);
+      }
       const int pos = it.c - it.n + it.t * kRows + r;                    // causal limit of this row
       const int warp_pos_min = it.c - it.n + it.t * kRows + (warp & 3) * 32;
       float m_used = -INFINITY;   // reference max of this row (log2 domain)
@@ -633,6 +690,9 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         if (lane == 0) mbar_arrive(p_full(g));
       }
       if (!ok) break;
+      if constexpr (kCvtQ) {
+        if (more && !(ok = convert_q(itc + 1))) break;
+      }
       // epilogue: once the item's last PV has completed, O / l -> out
       ok = !abort_sh && mbar_wait_bounded(pv_done(g), itc & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -645,7 +705,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int lr = it.t * kRows + r;
-      TO* orow = static_cast<TO*>(a.out) + ((static_cast<size_t>(it.q0) + lr) * H + it.h + g) * D;
+      TA* orow = static_cast<TA*>(a.out) + ((static_cast<size_t>(it.q0) + lr) * H + it.h + g) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
@@ -654,10 +714,10 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 v;
-            v.x = Mma<TO>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
-            v.y = Mma<TO>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
-            v.z = Mma<TO>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
-            v.w = Mma<TO>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
+            v.x = Mma<TA>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
+            v.y = Mma<TA>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
+            v.z = Mma<TA>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
+            v.w = Mma<TA>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
             reinterpret_cast<uint4*>(orow + cc * 32)[e] = v;
           }
         }
@@ -668,6 +728,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       ++k;
     }
     if (!ok) abort_sh = 1;
+    if (kCvtQ && (range & 0x80008000u)) flag_status(a.status, PA_DEV_RANGE);
     teardown();
     if (threadIdx.x == 0 && abort_sh) flag_status(a.status, PA_DEV_WAIT_TIMEOUT);
     if (warp == 0) {
@@ -682,11 +743,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 }
 
 namespace {
-template <typename T, typename TO, int D>
+template <typename T, typename TA, int D>
 cudaError_t launch_umma_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const CUtensorMap& qmap, cudaStream_t stream) {
   const int smem = UmmaLayout<D>::SMEM + 1024;
-  auto kern = prefill_umma_kernel<T, TO, D>;
+  auto kern = prefill_umma_kernel<T, TA, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM, or fewer when there are fewer items
@@ -700,18 +761,18 @@ cudaError_t launch_umma_t(const PrefillArgs& a, const CUtensorMap& kmap, const C
   return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream, kmap, vmap, qmap, a);
 }
 
-template <typename T, typename TO>
+template <typename T, typename TA>
 cudaError_t launch_umma_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const CUtensorMap& qmap, cudaStream_t stream) {
-  return a.head_dim == 128 ? launch_umma_t<T, TO, 128>(a, kmap, vmap, qmap, stream)
-                           : launch_umma_t<T, TO, 64>(a, kmap, vmap, qmap, stream);
+  return a.head_dim == 128 ? launch_umma_t<T, TA, 128>(a, kmap, vmap, qmap, stream)
+                           : launch_umma_t<T, TA, 64>(a, kmap, vmap, qmap, stream);
 }
 }  // namespace
 
-cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, int out_dtype, const CUtensorMap& kmap,
+cudaError_t launch_prefill_umma(const PrefillArgs& a, int dtype, int act_dtype, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& qmap, cudaStream_t stream) {
   if (dtype == PA_BF16) return launch_umma_d<__nv_bfloat16, __nv_bfloat16>(a, kmap, vmap, qmap, stream);
-  if (out_dtype == PA_BF16) return launch_umma_d<__half, __nv_bfloat16>(a, kmap, vmap, qmap, stream);
+  if (act_dtype == PA_BF16) return launch_umma_d<__half, __nv_bfloat16>(a, kmap, vmap, qmap, stream);
   return launch_umma_d<__half, __half>(a, kmap, vmap, qmap, stream);
 }
 

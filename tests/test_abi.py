@@ -108,21 +108,20 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
 def test_int8_prefill_validates_on_the_host(lib):
     """The INT8 prompt pass: the pool must be INT8 with a bf16/fp16 act_dtype,
     the workspace present and large enough.  The workspace is the fp16 K and V
-    copies of num_seqs x ceil(max_context_len / 16) blocks and their int32
-    block table (each part 256-byte aligned), and for bf16 activations an
-    fp16 copy of num_seqs x max_q_len rows of q (the pass stores the output
-    rows as bf16 itself)."""
+    copies of num_seqs x ceil(max_context_len / 16) blocks (each 256-byte
+    aligned) and their int32 block table, whatever the activations' type:
+    bf16 queries are converted and the output stored by the pass itself."""
     f = ctypes.c_void_p(FAKE)
     i8 = _desc(dt=B.PA_I8)
     al = lambda n: ((n + 255) // 256) * 256
     pool = 2 * 4 * 8 * 16 * 128 * 2                      # 2 seqs x 4 blocks x 8 heads x 16 x 128 x 2 bytes
-    rows = 2 * 64 * 32 * 128 * 2                         # 2 seqs x 64 rows x 32 heads x 128 x 2 bytes
-    f16 = lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_F16, ctypes.byref(i8))
-    assert f16 == 2 * al(pool) + 2 * 4 * 4
-    size = lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_BF16, ctypes.byref(i8))
-    assert size == 2 * al(pool) + al(2 * 4 * 4) + rows
-    assert lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_BF16, ctypes.byref(_desc(dt=B.PA_BF16))) == 0
-    assert lib.pa_prefill_int8_workspace_size(2, 32, 64, 64, B.PA_F32, ctypes.byref(i8)) == 0
+    size = lib.pa_prefill_int8_workspace_size(2, 64, ctypes.byref(i8))
+    assert size == 2 * al(pool) + 2 * 4 * 4
+    assert lib.pa_prefill_int8_workspace_size(2, 50, ctypes.byref(i8)) == size    # 50 tokens: 4 blocks too
+    assert lib.pa_prefill_int8_workspace_size(0, 64, ctypes.byref(i8)) == 0
+    assert lib.pa_prefill_int8_workspace_size(2, 64, ctypes.byref(_desc(dt=B.PA_BF16))) == 0
+    assert lib.pa_prefill_int8_workspace_size(-1, 64, ctypes.byref(i8)) == 0
+    f16 = size
     call = lambda desc, act=B.PA_BF16, ws=f, wsb=size, maxq=64, maxc=64, S=2: lib.pa_prefill_attention_int8(
         f, f, f, f, f, f, f, f, f, 0.1, S, 32, 4, maxq, maxc, act, ctypes.byref(desc), ws, wsb, None)
     assert call(_desc(dt=B.PA_BF16)) == B.PA_ERR_INVALID          # float pool
