@@ -445,6 +445,24 @@ def test_prefill_int8_bad_block_id_is_reported():
     assert torch.equal(out2[:40], out[:40]) and torch.equal(out2[110:], out[110:])   # sequences 0 and 2
 
 
+def test_prefill_int8_bf16_query_past_fp16_range_is_reported():
+    """The pass runs in fp16, so a bf16 query element of magnitude 2^16 or more
+    cannot be held: it is clamped to 65504 and PA_DEV_RANGE is set; every
+    other (row, head) output is what it was."""
+    wl, q, cu, ctx = _prefill8_case(153, [40, 70], [0, 30], 32, 8, 128, torch.bfloat16)
+    cache = Cache(wl)
+    out = _prefill8(wl, cache, q, cu, ctx)
+    assert pa.pa_device_status() == 0
+    q2 = q.clone()
+    q2[45, 3, 7] = 1.0e5                                  # sequence 1, its row 5, head 3
+    out2 = _prefill8(wl, cache, q2, cu, ctx)
+    assert pa.pa_device_status() & pa.PA_DEV_RANGE
+    assert torch.isfinite(out2.float()).all()
+    same = torch.ones(out.shape[:2], dtype=torch.bool)
+    same[45, 3] = False
+    assert torch.equal(out2[same.to(DEV)], out[same.to(DEV)])
+
+
 def test_prefill_int8_matches_the_float_pass_on_its_dequantised_pools():
     """Consistency check, not parity evidence: on a cache whose x_hat is exactly
     representable in fp16 (power-of-two scales, 8-bit codes), the INT8 prompt
