@@ -115,6 +115,55 @@ def test_append_int8_special_rows():
     assert pa.pa_device_status() & pa.PA_DEV_BAD_SLOT
 
 
+def _near_tie_rows(dtype, amaxes, d):
+    """One row per amax A: A itself and the d - 1 values of `dtype` in
+    [-A, A] whose quotient by s = float32(A / 127) lies closest to a
+    half-integer (where the rounding of x / s decides the code), so that the
+    quantiser's rounding test meets values on both sides of its margin."""
+    if dtype == torch.float16:
+        every = torch.arange(0, 0x7c00, dtype=torch.int32).to(torch.int16).view(torch.float16)
+    else:
+        every = torch.arange(0, 0x7f80, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    vals = every.double().numpy()
+    rows = []
+    for a in amaxes:
+        a = float(torch.tensor(a, dtype=dtype).double())
+        sc = np.float64(np.float32(np.float32(a) / np.float32(127)))
+        cand = np.concatenate([vals[vals <= a], -vals[(vals > 0) & (vals <= a)]])
+        q = cand / sc
+        dist = np.abs(q - np.floor(q) - 0.5)
+        pick = cand[np.argsort(dist, kind="stable")[:d - 1]]
+        rows.append(np.concatenate([[a], pick]))
+    return torch.tensor(np.array(rows)).to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_append_int8_near_ties(dtype):
+    """Codes of values whose x / s sits within a few ulps of k + 1/2 for
+    inexact scales: bit-exact against the oracle's float32 division."""
+    hkv, d = 2, 128
+    amaxes = [100.0, 77.3, 1.7, 0.013, 3.1e-4, 6.0e-5, 5.5e4]
+    rows = _near_tie_rows(dtype, amaxes, d)               # [len(amaxes)][d]
+    T = len(amaxes)
+    xk = torch.zeros((T, hkv, d), dtype=dtype)
+    xk[:, 0] = rows
+    xk[:, 1] = rows.flip(1)
+    xv = torch.roll(xk, 1, dims=0)
+    nb = 2
+    kc = torch.zeros((nb, hkv, 16, d), dtype=torch.int8)
+    ks = torch.zeros((nb, hkv, 16))
+    wl = W.Workload(name="near_ties", config_id=0, dtype=dtype, num_q_heads=2, num_kv_heads=hkv,
+                    head_dim=d, scale=0.1, steps=1, k_pool=kc, v_pool=kc.clone(),
+                    block_tables=torch.zeros((1, 1), dtype=torch.int32), ctx0=torch.zeros(1, dtype=torch.int32),
+                    decode_rows=slice(0, 1), k_scales=ks, v_scales=ks.clone())
+    cache = Cache(wl)
+    st = W.StepInputs(slot_mapping=torch.arange(T, dtype=torch.int64) * 3, k_new=xk, v_new=xv,
+                      q=torch.zeros((1, 2, d), dtype=dtype), context_lens=torch.zeros(1, dtype=torch.int32))
+    cache.append(st)
+    assert cache.same_as_oracle()
+    assert pa.pa_device_status() == 0
+
+
 def test_append_int8_llama3_8b_steps():
     wl = W.llama3_8b_decode(steps=3, kv="int8")
     cache = Cache(wl)
