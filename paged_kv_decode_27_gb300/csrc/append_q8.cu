@@ -10,9 +10,11 @@
 // loaded together, before the slot mapping is consulted, so a warp waits on
 // one load latency per group (up to eight heads; smaller groups when the
 // batch is too small to fill the GPU otherwise).  Each lane holds D/32
-// elements of a row, the row maximum is a warp reduction, and every lane
-// writes its D/32 codes (so the 128- or 64-byte code row is one coalesced
-// store) while lane 0 writes the float32 scale.
+// elements of each row; the eight rows' maxima come from one transposed
+// butterfly that leaves row u's on lanes 4u .. 4u + 3, which compute its
+// scale (so the division runs once for eight rows) and hand it to the other
+// lanes; every lane writes its D/32 codes (so the 128- or 64-byte code row
+// is one coalesced store) and lane 4u the float32 scale of row u.
 //
 // The scale is one IEEE division, s = amax / 127.  Each code is the
 // round-to-nearest-even of the IEEE quotient fl(x / s), decided without a
@@ -21,9 +23,9 @@
 // within that bound of a decision boundary): t = x * (1/s) with the
 // correctly rounded reciprocal is within 2^-16 of x / s for |x / s| <= 128,
 // and fl(x / s) within 2^-17, so when t lies more than 2^-12 from a
-// half-integer both round to the same integer; otherwise (and for a
-// non-finite t) the code takes the division itself.  Codes and scales are
-// bit-exact functions of the row.
+// half-integer both round to the same integer; when some element of a row
+// does not (or t is not finite), the warp recomputes that row's codes with
+// the division itself.  Codes and scales are bit-exact functions of the row.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -45,16 +47,25 @@ template <> struct Lanes<2> {   // D = 64: 4 bytes in, 2 codes out per lane
 
 constexpr int kHeadsPerPass = 8;
 
-// round-to-nearest-even of fl(x / s) clamped to [-127, 127], for s > 0 and
-// r = 1/s correctly rounded (see the rounding test above)
-__device__ __forceinline__ int code_of(float x, float s, float r) {
-  const float t = x * r;
-  const float f = t - floorf(t);   // within 2^-25 of the fraction of t
-  int c;
-  if (fabsf(t) < 256.f && fabsf(f - 0.5f) > 0x1p-12f)
-    c = __float2int_rn(t);
-  else
-    c = __float2int_rn(__fdiv_rn(x, s));
+// Round-to-nearest-even of t = x * r (r = 1/s correctly rounded, s > 0):
+// adding 1.5 * 2^23 leaves the nearest integer of |t| < 2^22 in the low
+// mantissa bits, and t minus that integer (both exact) is the rounding error
+// e in [-1/2, 1/2].  `near` is set when t is within the test's margin of a
+// half-integer (|e| within 2^-12 of 1/2) or not finite and small, i.e. when
+// the division has to decide.  The explicit-rounding intrinsics keep the
+// compiler from fusing the steps into FMAs.
+__device__ __forceinline__ int fast_code(float x, float r, bool& near) {
+  const float t = __fmul_rn(x, r);
+  const float m = __fadd_rn(t, 12582912.f);
+  const float e = __fsub_rn(t, __fsub_rn(m, 12582912.f));
+  near |= !(fabsf(t) < 256.f) || !(fabsf(fabsf(e) - 0.5f) > 0x1p-12f);
+  return __float_as_int(m) - 0x4B400000;
+}
+
+// the code itself: round-to-nearest-even of the IEEE quotient fl(x / s),
+// clamped to [-127, 127]
+__device__ __forceinline__ int exact_code(float x, float s) {
+  const int c = __float2int_rn(__fdiv_rn(x, s));
   return c > 127 ? 127 : (c < -127 ? -127 : c);
 }
 
@@ -81,8 +92,10 @@ append_q8_kernel(int8_t* __restrict__ k_codes, int8_t* __restrict__ v_codes, flo
   for (int h0 = h_begin; h0 < h_end; h0 += kHeadsPerPass) {
     In raw[kHeadsPerPass];
 #pragma unroll
-    for (int u = 0; u < kHeadsPerPass; ++u)
+    for (int u = 0; u < kHeadsPerPass; ++u) {
+      raw[u] = In{};
       if (h0 + u < h_end) raw[u] = __ldcs(reinterpret_cast<const In*>(src + static_cast<size_t>(h0 + u) * D));
+    }
     if (slot < 0) return;                                   // padding token
     if (slot >= static_cast<long long>(num_blocks) * kBlock) {
       if (lane == 0 && !is_v) flag_status(status, PA_DEV_BAD_SLOT);
@@ -90,30 +103,68 @@ append_q8_kernel(int8_t* __restrict__ k_codes, int8_t* __restrict__ v_codes, flo
     }
     const long long blk = slot / kBlock;
     const int off = static_cast<int>(slot - blk * kBlock);
+    // this lane's elements and the partial maxima of its 8 rows (0 for rows
+    // past the group)
+    float x[kHeadsPerPass][EPL];
+    float v[kHeadsPerPass];
+#pragma unroll
+    for (int u = 0; u < kHeadsPerPass; ++u) {
+      const T* e = reinterpret_cast<const T*>(&raw[u]);
+      v[u] = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        x[u][i] = h0 + u < h_end ? Elem<T>::to_f(e[i]) : 0.f;
+        v[u] = fmaxf(v[u], fabsf(x[u][i]));
+      }
+    }
+    // Row maxima by a transposed butterfly: at the exchanges over lane bits
+    // 4, 3 and 2 each lane keeps half of its rows and receives the partner's
+    // partial maxima of those rows, so that lane l ends with row
+    // (l >> 2) & 7, whose maximum the exchanges over bits 1 and 0 complete
+    // (9 shuffles for 8 rows).
+    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+    float w4[4], w2[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float keep = b4 ? v[4 + j] : v[j];
+      const float send = b4 ? v[j] : v[4 + j];
+      w4[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float keep = b3 ? w4[2 + j] : w4[j];
+      const float send = b3 ? w4[j] : w4[2 + j];
+      w2[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+    float amax = fmaxf(b2 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4));
+    amax = warp_max_xor(amax, 1, 2);
+    // the scale of row (lane >> 2) & 7 and its reciprocal: one division for
+    // the 8 rows
+    const float sc_l = __fdiv_rn(amax, 127.f);
+    const float rc_l = sc_l > 0.f ? __frcp_rn(sc_l) : 0.f;
+    const int my_row = (lane >> 2) & 7;
+    if ((lane & 3) == 0 && h0 + my_row < h_end)
+      scales[(static_cast<size_t>(blk) * num_kv_heads + h0 + my_row) * kBlock + off] = sc_l;
 #pragma unroll
     for (int u = 0; u < kHeadsPerPass; ++u) {
       const int h = h0 + u;
       if (h >= h_end) break;
-      const T* e = reinterpret_cast<const T*>(&raw[u]);
-      float x[EPL];
-      float amax = 0.f;
+      const float sc = __shfl_sync(0xffffffffu, sc_l, 4 * u);
+      const float rc = __shfl_sync(0xffffffffu, rc_l, 4 * u);
+      int c[EPL];
+      bool near = false;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        x[i] = Elem<T>::to_f(e[i]);
-        amax = fmaxf(amax, fabsf(x[i]));
+      for (int i = 0; i < EPL; ++i) c[i] = fast_code(x[u][i], rc, near);
+      if (__any_sync(0xffffffffu, near)) {   // rare: the row has a quotient near a tie
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) c[i] = exact_code(x[u][i], sc);
       }
-      amax = warp_max_xor(amax, 1, 16);
-      const float sc = __fdiv_rn(amax, 127.f);
-      const float rc = sc > 0.f ? __frcp_rn(sc) : 0.f;
       Out packed = 0;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int c = sc > 0.f ? code_of(x[i], sc, rc) : 0;
-        packed |= static_cast<Out>(static_cast<Out>(c & 0xff) << (8 * i));
-      }
+      for (int i = 0; i < EPL; ++i)
+        packed |= static_cast<Out>(static_cast<Out>((sc > 0.f ? c[i] : 0) & 0xff) << (8 * i));
       const size_t r = (static_cast<size_t>(blk) * num_kv_heads + h) * kBlock + off;
       reinterpret_cast<Out*>(codes + r * D)[lane] = packed;
-      if (lane == 0) scales[r] = sc;
     }
   }
 }
