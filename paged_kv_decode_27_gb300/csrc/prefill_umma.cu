@@ -597,18 +597,12 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     };
     bool ok = true;
     long long k = 0;
-    Item it;
+    Item it, nx;
+    bool have = find_item(k, it);
     if constexpr (kCvtQ) {
-      long long k0 = 0;
-      if (find_item(k0, it)) ok = convert_q(0);
+      if (have) ok = convert_q(0);
     }
-    while (ok && find_item(k, it)) {
-      bool more = false;   // convert mode: another item follows this one
-      if constexpr (kCvtQ) {
-        long long kn = k + 1;
-        Item nx;
-        more = find_item(kn, nx);
-      }
+    while (ok && have) {
       const int pos = it.c - it.n + it.t * kRows + r;                    // causal limit of this row
       const int warp_pos_min = it.c - it.n + it.t * kRows + (warp & 3) * 32;
       float m_used = -INFINITY;   // reference max of this row (log2 domain)
@@ -633,9 +627,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           for (int i = 0; i < kKeys; ++i) x[i] *= a.scale_log2;
         }
         if (diag) {
+          // keys key0 .. key0 + lim are visible to this row: a select per
+          // key (the rows of a warp differ, so a branch would diverge)
+          const int lim = pos - key0;
 #pragma unroll
-          for (int i = 0; i < kKeys; ++i)
-            if (key0 + i > pos) x[i] = -INFINITY;
+          for (int i = 0; i < kKeys; ++i) x[i] = i > lim ? -INFINITY : x[i];
         }
         float pm[8];
 #pragma unroll
@@ -690,8 +686,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         if (lane == 0) mbar_arrive(p_full(g));
       }
       if (!ok) break;
+      // the next item, looked up while this item's last PV runs
+      long long kn = k + 1;
+      const bool have_next = find_item(kn, nx);
       if constexpr (kCvtQ) {
-        if (more && !(ok = convert_q(itc + 1))) break;
+        if (have_next && !(ok = convert_q(itc + 1))) break;
       }
       // epilogue: once the item's last PV has completed, O / l -> out
       ok = !abort_sh && mbar_wait_bounded(pv_done(g), itc & 1);
@@ -725,7 +724,9 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free(g));
-      ++k;
+      k = kn;
+      it = nx;
+      have = have_next;
     }
     if (!ok) abort_sh = 1;
     if (kCvtQ && (range & 0x80008000u)) flag_status(a.status, PA_DEV_RANGE);
