@@ -22,10 +22,11 @@
 //   S_g = Q_g K^T  (M = 128 query rows, N = 128 keys, K = D; Q and K from
 //                   128-byte swizzled shared memory) into tensor memory;
 //   softmax        one thread per query row reads its row of S, applies the
-//                   causal mask and the online softmax (log2 domain, the
-//                   running reference raised lazily: only when a row's
-//                   maximum grows by more than 2^8), writes P (bf16/fp16
-//                   pairs) over S;
+//                   causal mask (a select per key on the diagonal tile: the
+//                   rows of a warp differ, a branch would diverge) and the
+//                   online softmax (log2 domain, the running reference raised
+//                   lazily: only when a row's maximum grows by more than
+//                   2^8), writes P (bf16/fp16 pairs) over S;
 //   O_g += P_g V   (M = 128, N = D, K = 128 keys; P from tensor memory, V read
 //                   MN-major straight from its pool layout).
 // One thread issues both tiles' products, interleaved so that one tile's
@@ -48,7 +49,9 @@
 // Warps (384 threads, three warpgroups that re-balance their registers with
 // setmaxnreg):
 //   0-3 / 4-7  softmax of tile A / B (thread r owns query row r), and at the
-//              end of an item the epilogue: normalise O and store the rows
+//              end of an item the epilogue: normalise O and store the rows;
+//              the next item is looked up (global loads) while the item's
+//              last PV runs
 //              (for bf16 queries over an fp16 pool, also the in-place
 //              conversion of the tile's next Q, done while the item's last
 //              PV runs, so that the next item's S overlaps the epilogue);
