@@ -19,6 +19,11 @@
 
 // Device status word (PA_DEV_* bits), one per device that loads the library.
 __device__ int g_pa_status = 0;
+// Work counters of the prompt pass's run-time schedule: kSchedSlots pairs
+// (items taken, CTAs finished), zero at load; each launch draws the next
+// pair in turn and its last CTA sets the pair back to zero.
+constexpr int kSchedSlots = 1024;
+__device__ int g_pa_prefill_sched[2 * kSchedSlots] = {};
 
 namespace {
 
@@ -107,6 +112,27 @@ int* status_ptr() {
     cache_ctx[dev] = pa::current_context();
   }
   return cache[dev];
+}
+
+// This launch's pair of schedule counters on the current device, or null.
+// Launches take the pairs in turn, so two launches share a pair only when
+// kSchedSlots launches of the prompt pass are in flight at once.
+int* prefill_sched_ptr() {
+  static std::mutex mu;
+  static int* cache[64] = {};
+  static void* cache_ctx[64] = {};
+  static unsigned next_slot[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev] || cache_ctx[dev] != pa::current_context()) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_prefill_sched) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+    cache_ctx[dev] = pa::current_context();
+  }
+  const unsigned slot = next_slot[dev]++ % kSchedSlots;
+  return cache[dev] + 2 * slot;
 }
 
 // SMs of the current device, or kDefaultSms when none is current.
@@ -619,6 +645,8 @@ int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_p
   a.num_blocks = pool->num_blocks;
   a.max_q_len = max_q_len;
   a.status = status;
+  a.sched = prefill_sched_ptr();
+  if (!a.sched) return fail(PA_ERR_CUDA, "no CUDA device / schedule counters unavailable");
   CUtensorMap kmap, vmap, qmap;
   int rc;
   if ((rc = pool_map(&kmap, k_pool, pool)) != PA_OK) return rc;
@@ -635,8 +663,8 @@ int prefill_launch(void* out, const void* q, const void* k_pool, const void* v_p
 // Checks shared by the prompt passes (pool already checked): returns PA_OK, or
 // the error of the first violated rule.  Sets *nothing when there is no work.
 int check_prefill_args(const void* out, const void* q, const int32_t* block_tables, const int32_t* cu_q_lens,
-                       const int32_t* context_lens, float scale, int num_seqs, int max_q_len, int max_context_len,
-                       bool* nothing) {
+                       const int32_t* context_lens, float scale, int num_seqs, int num_q_heads, int max_q_len,
+                       int max_context_len, bool* nothing) {
   *nothing = false;
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "scale must be finite");
   if (max_q_len < 0 || max_q_len > max_context_len)
@@ -651,6 +679,9 @@ int check_prefill_args(const void* out, const void* q, const int32_t* block_tabl
       (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return fail(PA_ERR_INVALID, "int32 arrays must be 4-byte aligned");
   if ((max_q_len + 63) / 64 > 0x7fffffff) return fail(PA_ERR_UNSUPPORTED, "max_q_len too large");
+  // the run-time schedule counts (query tile, sequence, head) items in int32
+  if (static_cast<long long>((max_q_len + 127) / 128) * num_seqs * num_q_heads > 0x7fff0000LL)
+    return fail(PA_ERR_UNSUPPORTED, "too many query tiles in one prompt pass");
   return PA_OK;
 }
 
@@ -686,7 +717,7 @@ int pa_prefill_attention(void* out, const void* q, const void* k_pool, const voi
   if ((rc = reject_int8(pool)) != PA_OK) return rc;
   if (pool->dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "prefill needs bf16 or fp16 pools");
   bool nothing;
-  if ((rc = check_prefill_args(out, q, block_tables, cu_q_lens, context_lens, scale, num_seqs, max_q_len,
+  if ((rc = check_prefill_args(out, q, block_tables, cu_q_lens, context_lens, scale, num_seqs, num_q_heads, max_q_len,
                                max_context_len, &nothing)) != PA_OK)
     return rc;
   if (nothing) return PA_OK;
@@ -723,7 +754,7 @@ int pa_prefill_attention_int8(void* out, const void* q, const void* k_codes, con
   if (rc != PA_OK) return rc;
   if ((rc = check_int8(pool, act_dtype)) != PA_OK) return rc;
   bool nothing;
-  if ((rc = check_prefill_args(out, q, block_tables, cu_q_lens, context_lens, scale, num_seqs, max_q_len,
+  if ((rc = check_prefill_args(out, q, block_tables, cu_q_lens, context_lens, scale, num_seqs, num_q_heads, max_q_len,
                                max_context_len, &nothing)) != PA_OK)
     return rc;
   if (nothing) return PA_OK;

@@ -55,6 +55,7 @@ struct PrefillArgs {
   int num_blocks;
   int max_q_len;
   int* status;
+  int* sched;   // the launch's pair of schedule counters (items taken, CTAs finished), zero on entry
 };
 
 // Record `msg` as the calling thread's pa_last_error() and return `code`.

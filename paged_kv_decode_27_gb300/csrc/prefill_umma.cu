@@ -88,6 +88,8 @@ constexpr int kThreads = 384;   // three warpgroups
 constexpr int kTmemCols = 512;
 constexpr int kMaxPairs = 384;    // (sequence, query tile) pairs sorted in shared memory
 constexpr int kMaxCost = 63;      // key tiles per query tile, for the sort's buckets (longer share the last)
+constexpr int kRing = 4;          // item indices published ahead by the query loader
+static_assert(kRing * 4 + 2 * kRing * 8 + 4 <= (kMaxCost + 1) * 4, "the item ring fits the sort's histogram");
 // Registers per thread after the warpgroups re-balance the launch's
 // 168 x 384 = 64512: (200 + 200 + 96) x 128 = 63488 <= 64512, so the
 // increases never wait for registers that are not there.
@@ -271,35 +273,58 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int t_max = (a.max_q_len + kRows - 1) / kRows;
   const long long n_items = sorted ? static_cast<long long>(n_pairs) * HG
                                    : static_cast<long long>(t_max) * a.num_seqs * HG;
-  // Items are dealt round by round, in snake order (round m gives CTA b the
-  // item m * grid + b, or m * grid + grid - 1 - b when m is odd), so that the
-  // CTA with the longest item of one round gets the shortest of the next.
-  // The first item of round m or later that has work; false when none is left.
-  auto find_item = [&](long long& m, Item& it) -> bool {
-    for (;; ++m) {
-      const long long k = m * gridDim.x + ((m & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
-      if (k >= n_items) return false;
-      it.h = static_cast<int>(k % HG) * NT;
-      if (sorted) {
-        const int p = pairs[k / HG];
-        it.s = p >> 16;
-        it.t = p & 0xffff;
-      } else {
-        const long long r = k / HG;
-        it.s = static_cast<int>(r % a.num_seqs);
-        it.t = t_max - 1 - static_cast<int>(r / a.num_seqs);
-      }
-      if (!seq_shape(it.s, it.q0, it.n, it.c)) continue;
-      if (it.t * kRows >= it.n) continue;
-      it.nkt = key_tiles(it.c, it.n, it.t);
-      return true;
+  // Items are handed out at run time, longest first: the query loader of a
+  // CTA takes the next item index from a global counter when its CTA has room
+  // for another, so a CTA that drew short items takes more of them (a
+  // longest-processing-time schedule, without knowing the items' times).  The
+  // loader publishes each index into a 4-entry ring in shared memory
+  // (kRing), read by the other roles in the same order; -1 ends the ring.
+  // item_at: item k of the list; false when it has no work.
+  auto item_at = [&](int k, Item& it) -> bool {
+    it.h = (k % HG) * NT;
+    if (sorted) {
+      const int p = pairs[k / HG];
+      it.s = p >> 16;
+      it.t = p & 0xffff;
+    } else {
+      const int r = k / HG;
+      it.s = r % a.num_seqs;
+      it.t = t_max - 1 - r / a.num_seqs;
     }
+    if (!seq_shape(it.s, it.q0, it.n, it.c)) return false;
+    if (it.t * kRows >= it.n) return false;
+    it.nkt = key_tiles(it.c, it.n, it.t);
+    return true;
+  };
+  // The ring lives where the sort's histogram was (free from here on).
+  int* ring = hist;
+  const uint32_t ring_bar = smem_u32(hist + kRing);   // item_full[kRing] item_empty[kRing], 8-byte aligned
+  auto item_full = [&](int i) { return ring_bar + 8u * i; };
+  auto item_empty = [&](int i) { return ring_bar + 8u * (kRing + i); };
+  // A reader's next item index from the ring (use: the reader's count of
+  // reads); the slot is handed back at once.  -2 when the wait gave up.
+  auto ring_read = [&](uint32_t& use, bool arrive) -> int {
+    const int i = static_cast<int>(use % kRing);
+    if (abort_sh || !mbar_wait_bounded(item_full(i), (use / kRing) & 1)) return -2;
+    const int k = *reinterpret_cast<volatile int*>(ring + i);
+    if (arrive) mbar_arrive(item_empty(i));
+    ++use;
+    return k;
   };
 
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
+  // every thread is done with the histogram: the ring's barriers take its place
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(item_full(i), 1);
+      mbar_init(item_empty(i), 3 + 4 * NT);   // K and V producers, issuer, every softmax warp
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
 
   // Each role branch starts by setting its warpgroup's registers (every warp
   // of a warpgroup takes the same setmaxnreg) and ends with the CTA-wide
@@ -321,18 +346,26 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // over the lanes (lane l holds blocks l, l+32, l+64, l+96 of the chunk).
       const bool is_k = warp == 8;
       const CUtensorMap* map = is_k ? &kmap : &vmap;
-      const uint32_t ring = is_k ? sK : sV;
+      const uint32_t ring_base = is_k ? sK : sV;
       const uint32_t nst = is_k ? kStagesK : kStagesV;
       const uint64_t policy = l2_policy_evict_last();   // the other heads of the group read these tiles too
       const int oob_row = a.num_blocks * a.num_kv_heads * kBlock;   // rows past the pool read as zero
       uint32_t kv = 0;       // tiles issued
       bool ok = true;
-      long long k = 0;
+      uint32_t use = 0;      // ring reads (lane 0)
       Item it;
       auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
       };
-      while (ok && find_item(k, it)) {
+      // the next item: lane 0 reads the ring, the warp shares the index
+      auto next = [&]() -> int {
+        int kk = lane == 0 ? ring_read(use, true) : 0;
+        kk = __shfl_sync(0xffffffffu, kk, 0);
+        if (kk >= 0) item_at(kk, it);
+        return kk;
+      };
+      int kc;
+      while (ok && (kc = next()) >= 0) {
         const int kvh = it.h / G;
         const int nblk = it.nkt * kBlocksPerTile;
         int yr[4];
@@ -376,11 +409,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             ok = false;
             break;
           }
-          load_tile(map, ring + st * L::KT_BYTES, is_k ? k_full(st) : v_full(st), j);
+          load_tile(map, ring_base + st * L::KT_BYTES, is_k ? k_full(st) : v_full(st), j);
           ++kv;
         }
-        ++k;
       }
+      if (kc == -2) ok = false;
       if (!ok) {
         abort_sh = 1;
         // let the copies still in flight (at most the last kStages of each
@@ -433,9 +466,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         int sk = 0, sv = 0;           // K / V ring stages of the next tile
         uint32_t pk = 0, pv = 0;      // and the phase parity of their full barriers
         bool ok = true;
-        long long k = 0;
+        uint32_t use = 0;   // ring reads
         Item it;
-        while (ok && find_item(k, it)) {
+        int kc;
+        while (ok && (kc = ring_read(use, true)) >= 0) {
+          item_at(kc, it);
           ok = wait1(k_full(sk), pk);
           for (int g = 0; g < NT && ok; ++g) {
             if (!(ok = wait1(q_full(g), itc & 1))) break;
@@ -473,8 +508,8 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             if (++sv == kStagesV) { sv = 0; pv ^= 1u; }
           }
           ++itc;
-          ++k;
         }
+        if (kc == -2) ok = false;
         if (!ok) abort_sh = 1;
         umma_commit(mma_final(0));
         mbar_wait_bounded(mma_final(0), 0, 100000000ull);
@@ -492,9 +527,42 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       bool ok = true;
       uint32_t itc = 0;
       uint32_t tma_uses[2] = {0u, 0u};   // q_raw phases this warp started (convert mode)
-      long long k = 0;
+      // The schedule: lane 0 takes item indices from the global counter
+      // (skipping items without work) and publishes them into the ring, each
+      // once the Q tiles of the item before it are on their way; -1 once the
+      // counter has run out.
+      uint32_t pub = 0;   // indices published
+      auto fetch = [&]() -> int {
+        for (;;) {
+          const int kk = atomicAdd(a.sched, 1);
+          if (kk >= n_items) return -1;
+          Item x;
+          if (item_at(kk, x)) return kk;
+        }
+      };
+      auto publish = [&](int kk) -> bool {
+        const int i = static_cast<int>(pub % kRing);
+        if (pub >= kRing && (abort_sh || !mbar_wait_bounded(item_empty(i), ((pub / kRing) - 1) & 1))) return false;
+        *reinterpret_cast<volatile int*>(ring + i) = kk;
+        mbar_arrive(item_full(i));   // release: the readers' acquiring wait sees the index
+        ++pub;
+        return true;
+      };
+      auto fetch_publish = [&](int& kk) -> bool {
+        int ok1 = 1;
+        kk = -1;
+        if (lane == 0) {
+          kk = fetch();
+          ok1 = publish(kk) ? 1 : 0;
+        }
+        kk = __shfl_sync(0xffffffffu, kk, 0);
+        return __shfl_sync(0xffffffffu, ok1, 0) != 0;
+      };
       Item it;
-      while (ok && find_item(k, it)) {
+      int kc;
+      ok = fetch_publish(kc);
+      while (ok && kc >= 0) {
+        item_at(kc, it);
         for (int g = 0; g < NT && ok; ++g) {
           // the previous item's S products of this tile (its last reads of
           // Q_g) have completed
@@ -537,7 +605,12 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         }
         if (!ok) break;
         ++itc;
-        ++k;
+        // the next index once this item's Q tiles are on their way (the
+        // counter's round trip stays off their path; the readers want it
+        // only at this item's end)
+        int kn;
+        if (!(ok = fetch_publish(kn))) break;
+        kc = kn;
       }
       if (!ok) abort_sh = 1;
       if (kCvtQ && lane == 0) {
@@ -599,9 +672,16 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       return true;
     };
     bool ok = true;
-    long long k = 0;
-    Item it, nx;
-    bool have = find_item(k, it);
+    uint32_t use = 0;   // ring reads (lane 0 of each warp)
+    // the next item index: lane 0 of each warp reads the ring, the warp shares it
+    auto next = [&]() -> int {
+      int kk = lane == 0 ? ring_read(use, true) : 0;
+      return __shfl_sync(0xffffffffu, kk, 0);
+    };
+    Item it;
+    int kc = next();
+    bool have = kc >= 0;
+    if (have) item_at(kc, it);
     if constexpr (kCvtQ) {
       if (have) ok = convert_q(0);
     }
@@ -690,8 +770,8 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       }
       if (!ok) break;
       // the next item, looked up while this item's last PV runs
-      long long kn = k + 1;
-      const bool have_next = find_item(kn, nx);
+      const int kn = next();
+      const bool have_next = kn >= 0;
       if constexpr (kCvtQ) {
         if (have_next && !(ok = convert_q(itc + 1))) break;
       }
@@ -727,14 +807,26 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free(g));
-      k = kn;
-      it = nx;
+      kc = kn;
       have = have_next;
+      if (have) item_at(kc, it);
     }
+    if (kc == -2) ok = false;
     if (!ok) abort_sh = 1;
     if (kCvtQ && (range & 0x80008000u)) flag_status(a.status, PA_DEV_RANGE);
     teardown();
     if (threadIdx.x == 0 && abort_sh) flag_status(a.status, PA_DEV_WAIT_TIMEOUT);
+    if (threadIdx.x == 0) {
+      // the last CTA to finish returns the launch's counters to zero for the
+      // next launch that draws the same slot (every CTA's last take of an
+      // item index precedes its teardown, and so its count here)
+      __threadfence();
+      if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        a.sched[0] = 0;
+        a.sched[1] = 0;
+        __threadfence();
+      }
+    }
     if (warp == 0) {
       tc_fence_after_sync();
       tmem_dealloc(tmem, kTmemCols);
