@@ -83,3 +83,66 @@ def test_mixed_mistral7b_prefill_every_row():
                              st.cu_q_lens.numpy(), st.prefill_context_lens.numpy(), wl.scale)
     assert_close_to_ref(out, ref, wl.dtype, "mixed prefill")
     assert pa.pa_device_status() == 0
+
+
+def test_prefill_schedule_counters_wrap():
+    """Items are handed out at run time from one of 1024 per-launch counter
+    pairs, each set back to zero by its launch's last CTA.  1100 launches
+    wrap every pair at least once; the last output equals the first bit for
+    bit (an item's arithmetic does not depend on the CTA that runs it), and
+    the first matches the oracle."""
+    wl, q, cu, ctx = _case(71, [130, 257, 40], [0, 16, 300])
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    first = _run_prefill(wl, q, cu, ctx, kp, vp, wl.block_tables)
+    ref = oracle.prefill_ref(to_np(q), to_np(wl.k_pool), to_np(wl.v_pool), wl.block_tables.numpy(), cu.numpy(),
+                             ctx.numpy(), wl.scale)
+    assert_close_to_ref(first, ref, wl.dtype, "prefill, first launch")
+    out = torch.empty_like(first)
+    qd, btd, cud, ctxd = q.to(DEV), wl.block_tables.contiguous().to(DEV), cu.to(DEV), ctx.to(DEV)
+    for _ in range(1100):
+        pa.pa_prefill_attention(out, qd, kp, vp, btd, cud, ctxd, wl.scale, max_q_len=257,
+                                max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)
+    assert pa.pa_device_status() == 0
+
+
+def test_prefill_concurrent_launches_on_two_streams():
+    """Two prompt passes in flight at once on two streams draw different
+    counter pairs: each stays equal to its own single-stream result."""
+    cases = [_case(72, [300, 17], [0, 64]), _case(73, [129, 200, 64], [5, 0, 128], hq=16, hkv=2, d=64,
+                                                                           dtype=torch.float16)]
+    runs = []
+    for wl, q, cu, ctx in cases:
+        kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+        ref = _run_prefill(wl, q, cu, ctx, kp, vp, wl.block_tables)
+        runs.append((wl, q.to(DEV), cu.to(DEV), ctx.to(DEV), kp, vp, wl.block_tables.contiguous().to(DEV), ref,
+                     int((cu[1:] - cu[:-1]).max()), int(ctx.max())))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(r[7]) for r in runs]
+    for _ in range(50):
+        for (wl, q, cu, ctx, kp, vp, bt, _ref, mq, mc), st, o in zip(runs, streams, outs):
+            with torch.cuda.stream(st):
+                pa.pa_prefill_attention(o, q, kp, vp, bt, cu, ctx, wl.scale, max_q_len=mq, max_context_len=mc,
+                                        stream=st)
+    torch.cuda.synchronize()
+    for r, o in zip(runs, outs):
+        assert torch.equal(o, r[7])
+    assert pa.pa_device_status() == 0
+
+
+def test_prefill_many_sequences_unsorted_order():
+    """More (sequence, query tile) pairs than the sorted work list holds (384):
+    the items run in the fallback order over (tile, sequence, head group),
+    and the run-time schedule skips the items past each prompt.  400 short
+    prompts with cached prefixes, every row against the oracle."""
+    g = torch.Generator().manual_seed(74)
+    qlens = torch.randint(1, 150, (400,), generator=g).tolist()
+    prior = torch.randint(0, 40, (400,), generator=g).tolist()
+    wl, q, cu, ctx = _case(74, qlens, prior, hq=8, hkv=2, d=64, dtype=torch.bfloat16)
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    out = _run_prefill(wl, q, cu, ctx, kp, vp, wl.block_tables)
+    ref = oracle.prefill_ref(to_np(q), to_np(wl.k_pool), to_np(wl.v_pool), wl.block_tables.numpy(), cu.numpy(),
+                             ctx.numpy(), wl.scale)
+    assert_close_to_ref(out, ref, wl.dtype, "prefill, 400 sequences")
+    assert pa.pa_device_status() == 0
