@@ -16,7 +16,8 @@
 // this kernel once its MMAs are pipelined.  The grid is persistent (one CTA
 // per SM): each CTA sorts the (sequence, query tile) pairs by their number of
 // key tiles, longest first, in shared memory, and the items (a pair and a
-// head pair) are dealt to the CTAs round by round in snake order.
+// head pair) are handed out at run time in that order from a global counter,
+// each to the first CTA with room for it.
 //
 // Per K tile j of an item (128 keys = 8 pool blocks) and per tile g:
 //   S_g = Q_g K^T  (M = 128 query rows, N = 128 keys, K = D; Q and K from
