@@ -274,10 +274,11 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int t_max = (a.max_q_len + kRows - 1) / kRows;
   const long long n_items = sorted ? static_cast<long long>(n_pairs) * HG
                                    : static_cast<long long>(t_max) * a.num_seqs * HG;
-  // Items are handed out at run time, longest first: the query loader of a
-  // CTA takes the next item index from a global counter when its CTA has room
-  // for another, so a CTA that drew short items takes more of them (a
-  // longest-processing-time schedule, without knowing the items' times).  The
+  // Items are handed out at run time, longest first: CTA b starts with item
+  // b, and then the query loader of a CTA takes the next item index from a
+  // global counter when its CTA has room for another, so a CTA that drew
+  // short items takes more of them (a longest-processing-time schedule,
+  // without knowing the items' times).  The
   // loader publishes each index into a 4-entry ring in shared memory
   // (kRing), read by the other roles in the same order; -1 ends the ring.
   // item_at: item k of the list; false when it has no work.
@@ -533,9 +534,13 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // once the Q tiles of the item before it are on their way; -1 once the
       // counter has run out.
       uint32_t pub = 0;   // indices published
+      // CTA b's first item is item b (the counter starts past the grid), so
+      // the first tiles need no round trip to the counter
+      bool first = true;
       auto fetch = [&]() -> int {
         for (;;) {
-          const int kk = atomicAdd(a.sched, 1);
+          const int kk = first ? static_cast<int>(blockIdx.x) : atomicAdd(a.sched, 1) + static_cast<int>(gridDim.x);
+          first = false;
           if (kk >= n_items) return -1;
           Item x;
           if (item_at(kk, x)) return kk;
