@@ -90,7 +90,8 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxPairs = 384;    // (sequence, query tile) pairs sorted in shared memory
 constexpr int kMaxCost = 63;      // key tiles per query tile, for the sort's buckets (longer share the last)
 constexpr int kRing = 4;          // item indices published ahead by the query loader
-static_assert(kRing * 4 + 2 * kRing * 8 + 4 <= (kMaxCost + 1) * 4, "the item ring fits the sort's histogram");
+constexpr int kRingEntry = 8;     // ints per ring entry: index, then the item's s h t q0 n c nkt
+static_assert(kRing * kRingEntry * 4 + 2 * kRing * 8 <= (kMaxCost + 1) * 4, "the item ring fits the sort's histogram");
 // Registers per thread after the warpgroups re-balance the launch's
 // 168 x 384 = 64512: (200 + 200 + 96) x 128 = 63488 <= 64512, so the
 // increases never wait for registers that are not there.
@@ -279,8 +280,9 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   // global counter when its CTA has room for another, so a CTA that drew
   // short items takes more of them (a longest-processing-time schedule,
   // without knowing the items' times).  The
-  // loader publishes each index into a 4-entry ring in shared memory
-  // (kRing), read by the other roles in the same order; -1 ends the ring.
+  // loader publishes each item (its index and decoded fields) into a 4-entry
+  // ring in shared memory (kRing), read by the other roles in the same order,
+  // so no reader decodes an item from global memory; index -1 ends the ring.
   // item_at: item k of the list; false when it has no work.
   auto item_at = [&](int k, Item& it) -> bool {
     it.h = (k % HG) * NT;
@@ -300,19 +302,27 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   };
   // The ring lives where the sort's histogram was (free from here on).
   int* ring = hist;
-  const uint32_t ring_bar = smem_u32(hist + kRing);   // item_full[kRing] item_empty[kRing], 8-byte aligned
+  const uint32_t ring_bar = smem_u32(hist + kRing * kRingEntry);   // item_full[kRing] item_empty[kRing]
   auto item_full = [&](int i) { return ring_bar + 8u * i; };
   auto item_empty = [&](int i) { return ring_bar + 8u * (kRing + i); };
-  // A reader's next item index from the ring (use: the reader's count of
-  // reads); the slot is handed back at once.  -2 when the wait gave up.
-  auto ring_read = [&](uint32_t& use, bool arrive) -> int {
-    const int i = static_cast<int>(use % kRing);
-    if (abort_sh || !mbar_wait_bounded(item_full(i), (use / kRing) & 1)) return -2;
-    const int k = *reinterpret_cast<volatile int*>(ring + i);
-    if (arrive) mbar_arrive(item_empty(i));
-    ++use;
-    return k;
+  // A reader's read number `use`: every reading thread waits for the entry
+  // (bounded) and copies it; one thread per reading warp hands the slot back
+  // once the warp has read it.  ring_get returns the index (-1: the end).
+  auto ring_wait = [&](uint32_t use) -> bool {
+    return !abort_sh && mbar_wait_bounded(item_full(static_cast<int>(use % kRing)), (use / kRing) & 1);
   };
+  auto ring_get = [&](uint32_t use, Item& x) -> int {
+    const volatile int* e = ring + kRingEntry * static_cast<int>(use % kRing);
+    x.s = e[1];
+    x.h = e[2];
+    x.t = e[3];
+    x.q0 = e[4];
+    x.n = e[5];
+    x.c = e[6];
+    x.nkt = e[7];
+    return e[0];
+  };
+  auto ring_release = [&](uint32_t use) { mbar_arrive(item_empty(static_cast<int>(use % kRing))); };
 
   tc_fence_before_sync();
   __syncthreads();
@@ -354,16 +364,18 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       const int oob_row = a.num_blocks * a.num_kv_heads * kBlock;   // rows past the pool read as zero
       uint32_t kv = 0;       // tiles issued
       bool ok = true;
-      uint32_t use = 0;      // ring reads (lane 0)
+      uint32_t use = 0;      // ring reads
       Item it;
       auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, !abort_sh && mbar_wait_bounded(bar, parity)) != 0;
       };
-      // the next item: lane 0 reads the ring, the warp shares the index
+      // the next item from the ring, read by the whole warp
       auto next = [&]() -> int {
-        int kk = lane == 0 ? ring_read(use, true) : 0;
-        kk = __shfl_sync(0xffffffffu, kk, 0);
-        if (kk >= 0) item_at(kk, it);
+        if (!__all_sync(0xffffffffu, ring_wait(use))) return -2;
+        const int kk = ring_get(use, it);
+        __syncwarp();
+        if (lane == 0) ring_release(use);
+        ++use;
         return kk;
       };
       int kc;
@@ -471,8 +483,14 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         uint32_t use = 0;   // ring reads
         Item it;
         int kc;
-        while (ok && (kc = ring_read(use, true)) >= 0) {
-          item_at(kc, it);
+        auto next = [&]() -> int {
+          if (!ring_wait(use)) return -2;
+          const int kk = ring_get(use, it);
+          ring_release(use);
+          ++use;
+          return kk;
+        };
+        while (ok && (kc = next()) >= 0) {
           ok = wait1(k_full(sk), pk);
           for (int g = 0; g < NT && ok; ++g) {
             if (!(ok = wait1(q_full(g), itc & 1))) break;
@@ -537,38 +555,52 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // CTA b's first item is item b (the counter starts past the grid), so
       // the first tiles need no round trip to the counter
       bool first = true;
-      auto fetch = [&]() -> int {
+      auto fetch = [&](Item& x) -> int {
         for (;;) {
           const int kk = first ? static_cast<int>(blockIdx.x) : atomicAdd(a.sched, 1) + static_cast<int>(gridDim.x);
           first = false;
           if (kk >= n_items) return -1;
-          Item x;
           if (item_at(kk, x)) return kk;
         }
       };
-      auto publish = [&](int kk) -> bool {
+      auto publish = [&](int kk, const Item& x) -> bool {
         const int i = static_cast<int>(pub % kRing);
         if (pub >= kRing && (abort_sh || !mbar_wait_bounded(item_empty(i), ((pub / kRing) - 1) & 1))) return false;
-        *reinterpret_cast<volatile int*>(ring + i) = kk;
-        mbar_arrive(item_full(i));   // release: the readers' acquiring wait sees the index
+        volatile int* e = ring + kRingEntry * i;
+        e[0] = kk;
+        e[1] = x.s;
+        e[2] = x.h;
+        e[3] = x.t;
+        e[4] = x.q0;
+        e[5] = x.n;
+        e[6] = x.c;
+        e[7] = x.nkt;
+        mbar_arrive(item_full(i));   // release: the readers' acquiring wait sees the entry
         ++pub;
         return true;
       };
-      auto fetch_publish = [&](int& kk) -> bool {
+      // lane 0 takes and publishes the next item; the warp shares it
+      auto fetch_publish = [&](int& kk, Item& x) -> bool {
         int ok1 = 1;
         kk = -1;
         if (lane == 0) {
-          kk = fetch();
-          ok1 = publish(kk) ? 1 : 0;
+          kk = fetch(x);
+          ok1 = publish(kk, x) ? 1 : 0;
         }
         kk = __shfl_sync(0xffffffffu, kk, 0);
+        x.s = __shfl_sync(0xffffffffu, x.s, 0);
+        x.h = __shfl_sync(0xffffffffu, x.h, 0);
+        x.t = __shfl_sync(0xffffffffu, x.t, 0);
+        x.q0 = __shfl_sync(0xffffffffu, x.q0, 0);
+        x.n = __shfl_sync(0xffffffffu, x.n, 0);
+        x.c = __shfl_sync(0xffffffffu, x.c, 0);
+        x.nkt = __shfl_sync(0xffffffffu, x.nkt, 0);
         return __shfl_sync(0xffffffffu, ok1, 0) != 0;
       };
-      Item it;
+      Item it{}, nx{};
       int kc;
-      ok = fetch_publish(kc);
+      ok = fetch_publish(kc, it);
       while (ok && kc >= 0) {
-        item_at(kc, it);
         for (int g = 0; g < NT && ok; ++g) {
           // the previous item's S products of this tile (its last reads of
           // Q_g) have completed
@@ -615,8 +647,9 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         // counter's round trip stays off their path; the readers want it
         // only at this item's end)
         int kn;
-        if (!(ok = fetch_publish(kn))) break;
+        if (!(ok = fetch_publish(kn, nx))) break;
         kc = kn;
+        it = nx;
       }
       if (!ok) abort_sh = 1;
       if (kCvtQ && lane == 0) {
@@ -678,16 +711,19 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       return true;
     };
     bool ok = true;
-    uint32_t use = 0;   // ring reads (lane 0 of each warp)
-    // the next item index: lane 0 of each warp reads the ring, the warp shares it
-    auto next = [&]() -> int {
-      int kk = lane == 0 ? ring_read(use, true) : 0;
-      return __shfl_sync(0xffffffffu, kk, 0);
+    uint32_t use = 0;   // ring reads
+    // the next item from the ring, read by the whole warp
+    auto next = [&](Item& x) -> int {
+      if (!__all_sync(0xffffffffu, ring_wait(use))) return -2;
+      const int kk = ring_get(use, x);
+      __syncwarp();
+      if (lane == 0) ring_release(use);
+      ++use;
+      return kk;
     };
-    Item it;
-    int kc = next();
+    Item it, nx;
+    int kc = next(it);
     bool have = kc >= 0;
-    if (have) item_at(kc, it);
     if constexpr (kCvtQ) {
       if (have) ok = convert_q(0);
     }
@@ -776,7 +812,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       }
       if (!ok) break;
       // the next item, looked up while this item's last PV runs
-      const int kn = next();
+      const int kn = next(nx);
       const bool have_next = kn >= 0;
       if constexpr (kCvtQ) {
         if (have_next && !(ok = convert_q(itc + 1))) break;
@@ -815,7 +851,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       if (lane == 0) mbar_arrive(o_free(g));
       kc = kn;
       have = have_next;
-      if (have) item_at(kc, it);
+      it = nx;
     }
     if (kc == -2) ok = false;
     if (!ok) abort_sh = 1;
