@@ -679,6 +679,7 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     // S_g(j) of the last tile completes after every earlier product of the
     // single issuing thread (PV(j - 1) of both tiles included)
     const bool releaser = g == NT - 1 && (warp & 3) == 0 && lane == 0;
+    const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;   // rows of D >= 64 elements start 32-byte aligned
     // bf16 queries for an fp16 pass: the tile's 128 threads convert its Q
     // tile in place once it has landed (q_raw) and complete q_full -- the
     // first item's before its loop, each next item's while the current
@@ -835,14 +836,21 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         float o[32];
         tmem_ld32(tO + cc * 32, o);
         if (lr < it.n) {
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 v;
-            v.x = Mma<TA>::pack(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
-            v.y = Mma<TA>::pack(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
-            v.z = Mma<TA>::pack(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
-            v.w = Mma<TA>::pack(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
-            reinterpret_cast<uint4*>(orow + cc * 32)[e] = v;
+          for (int e = 0; e < 16; ++e) w[e] = Mma<TA>::pack(o[2 * e] * inv, o[2 * e + 1] * inv);
+          if (out32) {
+            // whole 32-byte sectors per store (the rows are 32-byte aligned when out is)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + cc * 32 + 16 * e),
+                           "r"(w[8 * e]), "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]), "r"(w[8 * e + 4]),
+                           "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
+                           : "memory");
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              reinterpret_cast<uint4*>(orow + cc * 32)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
         }
       }

@@ -146,3 +146,21 @@ def test_prefill_many_sequences_unsorted_order():
                              ctx.numpy(), wl.scale)
     assert_close_to_ref(out, ref, wl.dtype, "prefill, 400 sequences")
     assert pa.pa_device_status() == 0
+
+
+def test_prefill_output_only_16_byte_aligned():
+    """The epilogue stores whole 32-byte sectors when the output is 32-byte
+    aligned and 16-byte vectors otherwise: an output view 16 bytes past an
+    aligned base takes the second path and equals the first bit for bit."""
+    wl, q, cu, ctx = _case(75, [200, 64, 1], [0, 30, 7])
+    kp, vp = wl.k_pool.to(DEV), wl.v_pool.to(DEV)
+    aligned = _run_prefill(wl, q, cu, ctx, kp, vp, wl.block_tables)
+    assert aligned.data_ptr() % 32 == 0
+    base = torch.empty(aligned.numel() + 8, dtype=aligned.dtype, device=DEV)
+    shifted = base[8:].view(aligned.shape)
+    assert shifted.data_ptr() % 32 == 16
+    pa.pa_prefill_attention(shifted, q.to(DEV), kp, vp, wl.block_tables.contiguous().to(DEV), cu.to(DEV),
+                            ctx.to(DEV), wl.scale, max_q_len=200, max_context_len=int(ctx.max()))
+    torch.cuda.synchronize()
+    assert torch.equal(shifted, aligned)
+    assert pa.pa_device_status() == 0
