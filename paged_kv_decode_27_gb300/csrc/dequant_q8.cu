@@ -77,6 +77,7 @@ __device__ __forceinline__ void dequant_block(const DequantQ8Args& a, int s, int
   const size_t src0 = static_cast<size_t>(live ? id : 0) * a.num_kv_heads * kBlock;   // first row of the block
   const size_t dst0 = ob * a.num_kv_heads * kBlock;
   const int valid = c - lb * kBlock;                      // rows of the block inside the context
+  const bool out32 = ((reinterpret_cast<uintptr_t>(a.k_out) | reinterpret_cast<uintptr_t>(a.v_out)) & 31u) == 0;
   bool out_of_range = false;
   for (int base = 0; base < 2 * per_block; base += kUnrollBlock * blockDim.x) {
     uint4 w[kUnrollBlock];
@@ -109,8 +110,15 @@ __device__ __forceinline__ void dequant_block(const DequantQ8Args& a, int s, int
       widen16(w[u], sc[u], lo, hi, out_of_range);
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(is_k ? a.k_out : a.v_out) + (dst0 + row) * a.head_dim) +
                    2 * (j - row * chunks);
-      dst[0] = lo;
-      dst[1] = hi;
+      if (out32) {
+        // one whole 32-byte sector (the copies are 32-byte aligned when their base is)
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(lo.x), "r"(lo.y), "r"(lo.z),
+                     "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                     : "memory");
+      } else {
+        dst[0] = lo;
+        dst[1] = hi;
+      }
     }
   }
   if (out_of_range) flag_status(a.status, PA_DEV_RANGE);

@@ -494,6 +494,27 @@ def test_prefill_int8_bad_block_id_is_reported():
     assert torch.equal(out2[:40], out[:40]) and torch.equal(out2[110:], out[110:])   # sequences 0 and 2
 
 
+def test_prefill_int8_workspace_only_16_byte_aligned():
+    """The dequantisation stores whole 32-byte sectors when the workspace is
+    32-byte aligned and 16-byte vectors otherwise: a workspace view 16 bytes
+    past an aligned base gives the same output bit for bit."""
+    wl, q, cu, ctx = _prefill8_case(154, [70, 130], [20, 0], 32, 8, 128, torch.bfloat16)
+    cache = Cache(wl)
+    ref = _prefill8(wl, cache, q, cu, ctx)
+    need = pa.pa_prefill_int8_workspace_size(len(ctx), int(ctx.max()), cache.kc)
+    base = torch.empty(need + 32, dtype=torch.uint8, device=DEV)
+    ws = base[16:16 + need]
+    assert ws.data_ptr() % 32 == 16
+    out = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    qlens = cu[1:] - cu[:-1]
+    pa.pa_prefill_attention_int8(out, q.to(DEV), cache.kc, cache.vc, cache.ks, cache.vs,
+                                 wl.block_tables.contiguous().to(DEV), cu.to(DEV), ctx.to(DEV), wl.scale,
+                                 max_q_len=int(qlens.max()), max_context_len=int(ctx.max()), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert pa.pa_device_status() == 0
+
+
 def test_prefill_int8_bf16_query_past_fp16_range_is_reported():
     """The pass runs in fp16, so a bf16 query element of magnitude 2^16 or more
     cannot be held: it is clamped to 65504 and PA_DEV_RANGE is set; every
