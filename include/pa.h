@@ -259,7 +259,14 @@ PA_API int pa_verify_attention(void* out, const void* q, const void* k_pool, con
  *   max_q_len     : host-known max of q_len_s (sizes the grid)
  *   max_context_len : host-known max of context_lens (<= max_blocks_per_seq*16)
  * Errors as pa_decode_attention; fp32 pools are PA_ERR_UNSUPPORTED here (the
- * prompt pass runs on bf16/fp16 tensor cores).
+ * prompt pass runs on bf16/fp16 tensor cores), as is a call with more than
+ * ~2^31 (query tile, sequence, head) items.
+ * Scheduling: the (query tile, head pair) items are handed out at run time
+ * from a pair of device counters owned by the library.  Each call takes the
+ * next of 1024 pairs per device in turn, and the call's last CTA sets its pair
+ * back to zero.  Calls may overlap on different streams as long as fewer than
+ * 1024 prompt passes (of this and the INT8 entry point) are in flight at once
+ * on one device.
  */
 PA_API int pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
                          const int32_t* block_tables, const int32_t* cu_q_lens,
