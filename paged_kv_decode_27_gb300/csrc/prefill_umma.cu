@@ -45,14 +45,14 @@
 //
 // Tensor memory (512 columns): per tile S/P (128 columns) and O (D columns).
 // Shared memory: Q_A, Q_B, a 2-stage K ring and a 3-stage V ring, the sorted
-// work list.
+// work list (its histogram space then holds the ring of published items).
 //
 // Warps (384 threads, three warpgroups that re-balance their registers with
 // setmaxnreg):
 //   0-3 / 4-7  softmax of tile A / B (thread r owns query row r), and at the
-//              end of an item the epilogue: normalise O and store the rows;
-//              the next item is looked up (global loads) while the item's
-//              last PV runs
+//              end of an item the epilogue: normalise O and store the rows
+//              (32-byte stores when the output is 32-byte aligned); the next
+//              item is taken from the ring while the item's last PV runs
 //              (for bf16 queries over an fp16 pool, also the in-place
 //              conversion of the tile's next Q, done while the item's last
 //              PV runs, so that the next item's S overlaps the epilogue);
@@ -60,9 +60,11 @@
 //              block table);
 //   9          MMA issuer of both tiles (lane 0 alone), in the interleaved
 //              order below;
-//   11         query loader: the next item's Q tiles (TMA; cp.async for a
-//              prompt's last partial tile), once the current item's S
-//              products have completed.
+//   11         query loader and scheduler: takes the items (the first by
+//              CTA index, the rest from the global counter), publishes them
+//              decoded into the ring, and loads each item's Q tiles (TMA;
+//              cp.async for a prompt's last partial tile) once the previous
+//              item's S products have completed.
 // Every hand-off is an mbarrier; every wait is bounded, and a timeout sets
 // PA_DEV_WAIT_TIMEOUT, lets the copies and MMAs in flight finish (bounded)
 // and frees the tensor memory.
@@ -279,10 +281,10 @@ prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   // b, and then the query loader of a CTA takes the next item index from a
   // global counter when its CTA has room for another, so a CTA that drew
   // short items takes more of them (a longest-processing-time schedule,
-  // without knowing the items' times).  The
-  // loader publishes each item (its index and decoded fields) into a 4-entry
-  // ring in shared memory (kRing), read by the other roles in the same order,
-  // so no reader decodes an item from global memory; index -1 ends the ring.
+  // without knowing the items' times).  The loader publishes each item (its
+  // index and decoded fields) into a 4-entry ring in shared memory (kRing),
+  // read by the other roles in the same order, so no reader decodes an item
+  // from global memory; index -1 ends the ring.
   // item_at: item k of the list; false when it has no work.
   auto item_at = [&](int k, Item& it) -> bool {
     it.h = (k % HG) * NT;
