@@ -266,7 +266,8 @@ PA_API int pa_verify_attention(void* out, const void* q, const void* k_pool, con
  * next of 1024 pairs per device in turn, and the call's last CTA sets its pair
  * back to zero.  Calls may overlap on different streams as long as fewer than
  * 1024 prompt passes (of this and the INT8 entry point) are in flight at once
- * on one device.
+ * on one device.  A call captured into a CUDA graph keeps the pair it drew at
+ * capture: replays of one graph run one after another, not concurrently.
  */
 PA_API int pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
                          const int32_t* block_tables, const int32_t* cu_q_lens,
