@@ -103,6 +103,12 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert call(_desc(), maxq=65) == B.PA_ERR_INVALID
     assert call(_desc(), maxc=65) == B.PA_ERR_INVALID
     assert call(_desc(), out=ctypes.c_void_p(0)) == B.PA_ERR_INVALID
+    # the run-time schedule counts (query tile, sequence, head) items in
+    # int32: 65535 sequences x 64 heads x 512 tiles of 128 rows is refused
+    big = lib.pa_prefill_attention(f, f, f, f, f, f, f, 0.1, 65535, 64, 4096, 65536, 65536,
+                                   ctypes.byref(_desc()), None)
+    assert big == B.PA_ERR_UNSUPPORTED
+    assert "query tiles" in B.pa_last_error()
 
 
 def test_int8_prefill_validates_on_the_host(lib):
