@@ -48,18 +48,29 @@ template <> struct Lanes<2> {   // D = 64: 4 bytes in, 2 codes out per lane
 constexpr int kHeadsPerPass = 8;
 
 // Round-to-nearest-even of t = x * r (r = 1/s correctly rounded, s > 0):
-// adding 1.5 * 2^23 leaves the nearest integer of |t| < 2^22 in the low
-// mantissa bits, and t minus that integer (both exact) is the rounding error
-// e in [-1/2, 1/2].  `near` is set when t is within the test's margin of a
-// half-integer (|e| within 2^-12 of 1/2) or not finite and small, i.e. when
-// the division has to decide.  The explicit-rounding intrinsics keep the
-// compiler from fusing the steps into FMAs.
-__device__ __forceinline__ int fast_code(float x, float r, bool& near) {
+// adding 1.5 * 2^23 leaves the nearest integer n of |t| < 2^22 in the low
+// mantissa bits, so the low byte of the sum's bits is n in two's complement,
+// and t - n (both exact) is the rounding error e in [-1/2, 1/2].  A finite t
+// has |t| < 127.5 here (|x| <= amax, and r * amax = 127 within a few units in
+// the last place; a subnormal s below 2^-128 makes r infinite), so "t not
+// finite, or within the test's margin 2^-12 of a half-integer" is exactly
+// !(|e| < 1/2 - 2^-12): a non-finite t gives a NaN e.  `near` is set then,
+// when the division has to decide.  The explicit-rounding intrinsics keep
+// the compiler from fusing the steps into FMAs.  Returns the sum's bits.
+__device__ __forceinline__ uint32_t fast_code_bits(float x, float r, bool& near) {
   const float t = __fmul_rn(x, r);
   const float m = __fadd_rn(t, 12582912.f);
   const float e = __fsub_rn(t, __fsub_rn(m, 12582912.f));
-  near |= !(fabsf(t) < 256.f) || !(fabsf(fabsf(e) - 0.5f) > 0x1p-12f);
-  return __float_as_int(m) - 0x4B400000;
+  near |= !(fabsf(e) < 0.5f - 0x1p-12f);
+  return __float_as_uint(m);
+}
+
+// the low bytes of EPL words as EPL packed codes
+__device__ __forceinline__ uint32_t pack_codes(const uint32_t (&m)[4]) {
+  return __byte_perm(__byte_perm(m[0], m[1], 0x0040u), __byte_perm(m[2], m[3], 0x0040u), 0x5410u);
+}
+__device__ __forceinline__ uint16_t pack_codes(const uint32_t (&m)[2]) {
+  return static_cast<uint16_t>(__byte_perm(m[0], m[1], 0x0040u));
 }
 
 // the code itself: round-to-nearest-even of the IEEE quotient fl(x / s),
@@ -149,22 +160,20 @@ append_q8_kernel(int8_t* __restrict__ k_codes, int8_t* __restrict__ v_codes, flo
     for (int u = 0; u < kHeadsPerPass; ++u) {
       const int h = h0 + u;
       if (h >= h_end) break;
-      const float sc = __shfl_sync(0xffffffffu, sc_l, 4 * u);
+      // r = 0 when s = 0 (an all-zero row, or amax / 127 below the subnormal
+      // range): every finite element then gets code 0 on the fast path
       const float rc = __shfl_sync(0xffffffffu, rc_l, 4 * u);
-      int c[EPL];
+      uint32_t m[EPL];
       bool near = false;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) c[i] = fast_code(x[u][i], rc, near);
+      for (int i = 0; i < EPL; ++i) m[i] = fast_code_bits(x[u][i], rc, near);
       if (__any_sync(0xffffffffu, near)) {   // rare: the row has a quotient near a tie
+        const float sc = __shfl_sync(0xffffffffu, sc_l, 4 * u);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) c[i] = exact_code(x[u][i], sc);
+        for (int i = 0; i < EPL; ++i) m[i] = static_cast<uint32_t>(sc > 0.f ? exact_code(x[u][i], sc) : 0);
       }
-      Out packed = 0;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        packed |= static_cast<Out>(static_cast<Out>((sc > 0.f ? c[i] : 0) & 0xff) << (8 * i));
       const size_t r = (static_cast<size_t>(blk) * num_kv_heads + h) * kBlock + off;
-      reinterpret_cast<Out*>(codes + r * D)[lane] = packed;
+      reinterpret_cast<Out*>(codes + r * D)[lane] = pack_codes(m);
     }
   }
 }
