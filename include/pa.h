@@ -531,8 +531,8 @@ PA_API int pa_copy_blocks_int8(void* k_codes, void* v_codes, float* k_scales, fl
 
 /*
  * pa_decode_attention_noalloc -- pa_decode_attention for callers that cannot
- * allocate device memory.  (The paper has no counterpart: this entry point
- * exists for callers, not for the method.)
+ * allocate device memory.  (The method as described has no counterpart: this
+ * entry point exists for callers, not for the method.)
  *
  * Some callers cannot call cudaMalloc: a serving loop that may not allocate
  * once it is running, an embedder that hands over only tensors it already
