@@ -81,7 +81,7 @@ __device__ __forceinline__ int exact_code(float x, float s) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 append_q8_kernel(int8_t* __restrict__ k_codes, int8_t* __restrict__ v_codes, float* __restrict__ k_scales,
                  float* __restrict__ v_scales, const int64_t* __restrict__ slot_mapping,
                  const T* __restrict__ k_new, const T* __restrict__ v_new, int num_tokens, int num_kv_heads,
