@@ -3,9 +3,10 @@
 // Same work split as the tensor-core kernel -- grid (split, KV head, sequence),
 // W warps taking the partition's blocks round-robin, a shared-memory merge of
 // the warp states -- but each warp walks its blocks token by token with lanes
-// spread over the head dimension: a coalesced load of the K and V rows, one
-// warp-shuffle reduction per query head for the score, and an fp32 online
-// softmax update.  Used for fp32 pools, where tensor-core precision would not
+// spread over the head dimension: coalesced loads of the K and V rows (a
+// group of tokens at a time, so a block waits on a few load latencies, not
+// one per token), one warp-shuffle reduction per query head for the score,
+// and an fp32 online softmax update.  Used for fp32 pools, where tensor-core precision would not
 // meet the 1e-5 bar.
 #include "decode_merge.cuh"
 #include "pa_common.cuh"
@@ -99,24 +100,36 @@ __global__ void __launch_bounds__(W * 32) decode_simt_kernel(const DecodeArgs a)
     }
     const int nvalid = min(kBlock, ctx - lb * kBlock);
     const size_t tile = (static_cast<size_t>(id) * a.num_kv_heads + kvh) * kBlock * D;
-    for (int t = 0; t < nvalid; ++t) {
-      float kr[DPL], vr[DPL];
-      load_row_f<T, DPL>(kpool + tile + static_cast<size_t>(t) * D + lane * DPL, kr);
-      load_row_f<T, DPL>(vpool + tile + static_cast<size_t>(t) * D + lane * DPL, vr);
+    // TB tokens' K and V rows are loaded together (32 registers a lane), so a
+    // block costs kBlock / TB memory latencies instead of one per token; rows
+    // past the context lie inside the block's tile and are loaded but unused
+    constexpr int TB = 16 / DPL;
+    static_assert(kBlock % TB == 0, "token groups tile the block");
+    for (int t0 = 0; t0 < nvalid; t0 += TB) {
+      float kr[TB][DPL], vr[TB][DPL];
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        if (h < G) {
-          float x = 0.f;
+      for (int u = 0; u < TB; ++u) {
+        load_row_f<T, DPL>(kpool + tile + static_cast<size_t>(t0 + u) * D + lane * DPL, kr[u]);
+        load_row_f<T, DPL>(vpool + tile + static_cast<size_t>(t0 + u) * D + lane * DPL, vr[u]);
+      }
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) x = fmaf(qv[h][e], kr[e], x);
-          x = warp_sum_xor(x, 1, 16) * a.scale_log2;
-          const float mn = fmaxf(m[h], x);
-          const float al = exp2f(m[h] - mn);
-          const float p = exp2f(x - mn);
-          l[h] = l[h] * al + p;
+      for (int u = 0; u < TB; ++u) {
+        if (t0 + u >= nvalid) break;
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(acc[h][e], al, p * vr[e]);
-          m[h] = mn;
+        for (int h = 0; h < 8; ++h) {
+          if (h < G) {
+            float x = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) x = fmaf(qv[h][e], kr[u][e], x);
+            x = warp_sum_xor(x, 1, 16) * a.scale_log2;
+            const float mn = fmaxf(m[h], x);
+            const float al = exp2f(m[h] - mn);
+            const float p = exp2f(x - mn);
+            l[h] = l[h] * al + p;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(acc[h][e], al, p * vr[u][e]);
+            m[h] = mn;
+          }
         }
       }
     }
