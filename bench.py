@@ -575,10 +575,12 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.summary(t_busy0, t_wall1 + 0.1) if sampler else None
     # every configuration of the workload list, per call (L2 evicted), after the timed region
     configs = None
+    others = None
     if world == 1 and not args.quick:
         del kp, vp, dev_in, p_bufs, p_views, graphs
         torch.cuda.empty_cache()
         configs = measure_configs(pa, W, torch, dev)
+        others = measure_other_workloads(pa, W, torch, dev)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -606,6 +608,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks, "device_status": status,
         "cpu_baseline": cpu,
         "configs": configs,
+        "other_workloads": others,
     }
     print(json.dumps(line), flush=True)
 
@@ -624,6 +627,10 @@ N_LAYERS = {"tiny_fp32": 1, "llama32_1b_decode": 16, "llama3_8b_decode": 32, "pr
 # end of its decode range (batch 1 and 4 at contexts up to 8192).
 CONFIGS = ["tiny_fp32", "llama32_1b_decode", "llama3_8b_decode", "prefix_shared_8k", "mixed_mistral7b",
            "llama3_8b_long_b1", "llama3_8b_long_b4"]
+# The other calls of the path on the same head shapes: the INT8 cache (decode,
+# and the mixed step with its INT8 prompt pass) and the verification pass of
+# speculative decoding over both cache formats.
+OTHER_WORKLOADS = ["llama3_8b_decode_int8", "mixed_mistral7b_int8", "llama3_8b_verify", "llama3_8b_verify_int8"]
 
 
 def peak_bf16():
@@ -830,6 +837,20 @@ def measure_configs(pa, W, torch, dev, reps=60, warmup=5):
         res[name] = measure_workload(name, pa, W, torch, dev, reps, warmup, flush=flush)
         if name in ("llama32_1b_decode", "llama3_8b_long_b1", "llama3_8b_long_b4"):
             res[name]["model_step"] = measure_model_step(name, pa, W, torch, dev, max(reps // 3, 20), 3)
+        torch.cuda.empty_cache()
+    return res
+
+
+def measure_other_workloads(pa, W, torch, dev, reps=30, warmup=3):
+    """OTHER_WORKLOADS per call, as measure_configs; a workload that fails is
+    reported by its error, after the headline and the configurations."""
+    flush = l2_flusher(torch, dev)
+    res = {}
+    for name in OTHER_WORKLOADS:
+        try:
+            res[name] = measure_workload(name, pa, W, torch, dev, reps, warmup, flush=flush)
+        except Exception as e:   # keep the line: the headline was measured already
+            res[name] = {"error": repr(e)[:300]}
         torch.cuda.empty_cache()
     return res
 

@@ -91,3 +91,28 @@ def test_reference_arm_line_carries_the_contract_keys():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_other_workloads_report_a_failure_instead_of_ending_the_line(monkeypatch):
+    """The default line measures the INT8 and verification workloads after the
+    headline; one that raises is recorded by its error and the rest still run."""
+    sys.path.insert(0, ROOT)
+    import bench
+    seen = []
+
+    def fake_measure(name, pa, W, torch_mod, dev, reps, warmup, partition=0, flush=None):
+        seen.append(name)
+        if name == bench.OTHER_WORKLOADS[1]:
+            raise RuntimeError("synthetic failure")
+        return {"workload": name, "attention_us": 1.0}
+
+    monkeypatch.setattr(bench, "measure_workload", fake_measure)
+    monkeypatch.setattr(bench, "l2_flusher", lambda torch_mod, dev: None)
+    res = bench.measure_other_workloads(None, None, torch, torch.device("cpu"))
+    assert seen == bench.OTHER_WORKLOADS
+    assert "synthetic failure" in res[bench.OTHER_WORKLOADS[1]]["error"]
+    for name in bench.OTHER_WORKLOADS[:1] + bench.OTHER_WORKLOADS[2:]:
+        assert res[name]["attention_us"] == 1.0
+    from paged_kv_decode_27_gb300 import workloads as W
+    for name in bench.OTHER_WORKLOADS:
+        assert name in W.WORKLOADS and name in bench.N_LAYERS
